@@ -1,0 +1,110 @@
+/*
+ * spec_verify_oracle.h -- plain CPU oracle for lossless speculative verification.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load this library.  The GPU
+ * library never links, includes or calls it, and shares no code with it.
+ *
+ * Everything is computed in IEEE double, one row at a time, in the order the
+ * pages state the algorithm:
+ *   - accept draft x with probability min(1, p(x)/q(x)); on rejection resample
+ *     from max(p - q, 0) renormalised  (Uno article, "What 'lossless' actually
+ *     has to mean": the rule and Uno's _sparse_verify_tensors fragment);
+ *   - the block is truncated at the first rejection  (DFlash/DFlash2 guide,
+ *     4.4 "Mathematical Losslessness Guarantee");
+ *   - when all gamma drafts are accepted the target's bonus token is emitted,
+ *     so 1 <= emitted <= gamma + 1  (DFlash/DFlash2 guide, section 2
+ *     "Speculative Decoding Speedup Formulation");
+ *   - any-order variant: verify in generation order sigma, resample the first
+ *     rejected position from max(0, target - draft) and end the round
+ *     (Self-Speculative Masked Diffusions, key design 2).
+ *
+ * Readings where the pages are silent are listed with each function below.
+ */
+#ifndef SPEC_VERIFY_ORACLE_H
+#define SPEC_VERIFY_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+/* Per-row flag bits written to flags[b]. */
+enum {
+  ORACLE_FLAG_ACCEPT_BAND = 1u, /* some evaluated accept test had |u - min(1,p/q)| < 1e-6 */
+  ORACLE_FLAG_CDF_TIE = 2u,     /* emitted token's CDF boundary within 1e-6*T of u_s*T   */
+  ORACLE_FLAG_ZERO_RESID = 4u,  /* residual mass T <= 0 after a rejection: sampled from p */
+  ORACLE_FLAG_INPUT_ERR = 8u    /* invalid input row: n = -1, tokens = -1                 */
+};
+
+#define ORACLE_ACCEPT_BAND 1e-6 /* absolute, in units of the accept uniform          */
+#define ORACLE_TIE_BAND 1e-6    /* relative to T, i.e. in units of the sample uniform */
+
+/*
+ * Dense verification.
+ *   target_logits [B, gamma+1, V]   (dtype ORACLE_F32 or ORACLE_BF16 raw bits)
+ *   draft_logits  [B, gamma, V]
+ *   draft_ids     [B, gamma]  int32 in [0, V)
+ *   u_accept      [B, gamma]  fp32 in [0, 1)
+ *   u_sample      [B]         fp32 in [0, 1)
+ * Outputs (caller-owned host arrays):
+ *   n_accepted [B]; out_tokens [B, gamma+1] (x_0..x_{n-1}, resample/bonus, then -1)
+ *   residual_out [B, V] or NULL: the distribution the emitted token was drawn
+ *     from (r / T after a rejection, p_gamma for the bonus)
+ *   accept_prob [B, gamma] or NULL: min(1, p_j(x_j)/q_j(x_j)) for every j
+ *   resid_mass [B] or NULL: T (1 for a bonus draw, the sum of p_gamma)
+ *   flags [B] or NULL: ORACLE_FLAG_* bits
+ * Returns 0, or -1 on bad arguments / allocation failure.
+ */
+int oracle_verify_dense(const void* target_logits, const void* draft_logits, int dtype,
+                        const int32_t* draft_ids, const float* u_accept, const float* u_sample,
+                        int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                        double* residual_out, double* accept_prob, double* resid_mass,
+                        uint32_t* flags, int nthreads);
+
+/*
+ * Sparse top-k verification (Uno's sampler on (id, prob) support lists).
+ *   tgt_ids/tgt_probs [B, gamma+1, kt]  sorted strictly ascending by id
+ *   drf_ids/drf_probs [B, gamma, kd]    sorted strictly ascending by id
+ *   draft_tokens [B, gamma]; u_accept [B, gamma]; u_sample [B]
+ * Outputs as for dense; residual_out is [B, kt] (on the target support, list
+ * order).  p and q are the listed probabilities as given (no renormalisation);
+ * the draw after a rejection is over r = max(p - q_on_clean, 0) renormalised,
+ * the bonus draw is over the target list of position gamma normalised by its
+ * sum.
+ */
+int oracle_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,
+                         const int32_t* drf_ids, const float* drf_probs, int kd,
+                         const int32_t* draft_tokens, const float* u_accept, const float* u_sample,
+                         int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                         double* residual_out, double* accept_prob, double* resid_mass,
+                         uint32_t* flags, int nthreads);
+
+/*
+ * Any-order (masked-diffusion self-speculative) verification.
+ *   target_logits, draft_logits [B, D, V] in sequence-position order
+ *   order [B, W]: sigma, the window positions in verification order, a
+ *     permutation of W distinct positions in [0, D)
+ *   draft_tokens [B, D]; u_accept [B, W] (in window order); u_sample [B]
+ * Outputs: n_accepted [B] in [0, W]; out_tokens [B, D]: for window index i,
+ *   out[b, sigma_i] = draft token (i < n), resample (i == n), -1 (i > n);
+ *   positions outside the window are left untouched.  No bonus token.
+ *   residual_out [B, V] or NULL (zeros when n == W); accept_prob [B, W].
+ */
+int oracle_verify_anyorder(const void* target_logits, const void* draft_logits, int dtype,
+                           const int32_t* order, const int32_t* draft_tokens,
+                           const float* u_accept, const float* u_sample, int B, int D, int W,
+                           int V, int32_t* n_accepted, int32_t* out_tokens, double* residual_out,
+                           double* accept_prob, double* resid_mass, uint32_t* flags,
+                           int nthreads);
+
+/* Threads the oracle would use for nthreads <= 0 (all online host cores). */
+int oracle_default_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
