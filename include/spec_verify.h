@@ -1,0 +1,184 @@
+/*
+ * spec_verify.h -- C ABI of the GB300 batched lossless speculative-verification
+ * library (libspec_verify.so, CUDA kernels for sm_103a).
+ *
+ * The operation (Leviathan-style rejection sampling) as the pages state it:
+ *   - a drafter proposes gamma tokens x_j with distribution q_j; the target
+ *     scores every position in one parallel pass and gives p_j
+ *     (DFlash/DFlash2 guide, 4.4 "Mathematical Losslessness Guarantee");
+ *   - x_j is accepted with probability min(1, p_j(x_j)/q_j(x_j)); at the first
+ *     rejection the block is truncated and a replacement is drawn from the
+ *     renormalised residual max(p - q, 0)  (Uno article, "What 'lossless'
+ *     actually has to mean", and Uno's _sparse_verify_tensors fragment:
+ *     ratio = p/q where q > 0 else 0, accept iff u < min(1, ratio));
+ *   - if all gamma drafts are accepted the target's bonus token is drawn from
+ *     p_gamma, so every call emits between 1 and gamma + 1 tokens per row
+ *     (DFlash/DFlash2 guide, section 2, tau in [1, gamma + 1]);
+ *   - any-order variant: positions are verified in a generation order sigma,
+ *     the first rejection is resampled from max(0, target - draft) and ends
+ *     the round, no bonus token (Self-Speculative Masked Diffusions, key
+ *     design 2).
+ *
+ * Randomness is supplied by the caller: one accept uniform per draft position
+ * and one sample uniform per row, each in [0, 1).  For fixed inputs the
+ * results are a deterministic function of those uniforms: the inverse CDF
+ * walks the vocabulary (sparse: the sorted list) in ascending id order and
+ * returns the smallest id whose inclusive prefix mass exceeds u_sample * T.
+ *
+ * Conventions for every entry point
+ *   - All pointers are DEVICE pointers owned by the caller (cudaMalloc,
+ *     cudaMallocAsync or a framework allocator); the library allocates no
+ *     memory and keeps no global state.  Calls are asynchronous on `stream`
+ *     (the legacy default stream if 0).
+ *   - Tensors are dense, row-major, contiguous, with the shapes given below.
+ *     int32 / fp32 arrays need 4-byte alignment, bf16 arrays 2-byte
+ *     alignment.  Logit rows whose byte length is a multiple of 16, with
+ *     16-byte aligned base pointers, take the bulk-copy (TMA) fast path.
+ *   - Host-side argument errors (null pointers, non-positive sizes, sizes out
+ *     of range, a workspace that is too small) return SV_ERR_INVALID_ARG
+ *     synchronously and launch nothing.  A failed launch returns SV_ERR_CUDA.
+ *   - Device-side input errors (a draft id or sigma entry out of range, a
+ *     repeated sigma entry, an unsorted or repeated list id, a logit row that
+ *     contains NaN or +inf or is entirely -inf) do not stop the call: the
+ *     offending row gets n_accepted = -1 and out_tokens = -1, and a bit is
+ *     set in the workspace status word that spec_verify_check() reports.
+ *   - No kernel ever waits without a bound.  If a bounded wait runs out, the
+ *     call leaves its outputs undefined, sets the timeout bit, and the
+ *     workspace must be re-initialised with spec_verify_workspace_init().
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t (a CUstream_st pointer). */
+struct CUstream_st;
+typedef struct CUstream_st* sv_stream_t;
+
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_INVALID_ARG = 1,  /* rejected on the host, nothing launched           */
+  SV_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no GPU) */
+  SV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
+  SV_ERR_DEVICE_INPUT = 4, /* spec_verify_check: some row had invalid inputs   */
+  SV_ERR_TIMEOUT = 5       /* spec_verify_check: a bounded device wait ran out */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Largest sizes accepted by the entry points. */
+#define SV_MAX_VOCAB (1 << 24)
+#define SV_MAX_GAMMA 255  /* dense: gamma; any-order: W (and D <= SV_MAX_GAMMA * 64) */
+#define SV_MAX_LIST 4096  /* sparse: kt, kd */
+
+/* ABI version of this header; spec_verify_abi_version() returns it. */
+#define SV_ABI_VERSION 1
+int spec_verify_abi_version(void);
+
+/*
+ * Workspace: device scratch for the per-row counters, partial statistics and
+ * the status word.  spec_verify_workspace_size(B, gamma_or_W, V) bytes are
+ * enough for any of the three calls with those sizes (B rows, gamma drafts
+ * or a window of W, vocabulary V).  The workspace must be zeroed once before
+ * first use -- spec_verify_workspace_init() does that on `stream` -- and each
+ * successful call leaves its counters at zero again, so a call can be
+ * replayed (e.g. from a CUDA graph) without re-initialising.  One workspace
+ * must not be used by two calls that may run at the same time.
+ */
+size_t spec_verify_workspace_size(int B, int gamma_or_W, int V);
+sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * spec_verify_dense -- dense logits over the full vocabulary.
+ *   target_logits [B, gamma+1, V]  (dtype SV_F32 or SV_BF16); row j < gamma
+ *                                  scores draft j, row gamma is the bonus row
+ *   draft_logits  [B, gamma, V]    same dtype; may be NULL when gamma == 0
+ *   draft_ids     [B, gamma] int32 in [0, V): the drafted tokens x_j, which
+ *                                  must have been sampled from softmax(draft)
+ *   u_accept      [B, gamma] fp32 uniforms in [0, 1), one per draft
+ *   u_sample      [B]        fp32 uniform in [0, 1) for the one draw per row
+ * Outputs:
+ *   n_accepted    [B] int32: accepted drafts n in [0, gamma] (-1: bad input)
+ *   out_tokens    [B, gamma+1] int32: x_0..x_{n-1}, then the resampled token
+ *                 (n < gamma) or the bonus token (n == gamma), then -1
+ *   residual_out  [B, V] fp32 or NULL: the distribution the emitted token was
+ *                 drawn from (max(p_n - q_n, 0)/T, or p_gamma for the bonus)
+ *   accept_prob_out [B, gamma] fp32 or NULL: min(1, p_j(x_j)/q_j(x_j)) for
+ *                 every j (all positions are scored, as in the parallel pass)
+ * Softmax, gather, ratio test, first-reject scan and the inverse-CDF draw run
+ * in fp32 with fp64 combination of partial sums; bf16 inputs are widened
+ * exactly.  One fused persistent kernel reads each logit once from HBM.
+ */
+int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_ids, const float* u_accept, const float* u_sample,
+                      int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                      float* residual_out, float* accept_prob_out, void* workspace,
+                      size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * spec_verify_sparse -- Uno-style sparse support lists (Uno article, "What
+ * 'lossless' actually has to mean", _sparse_verify_tensors).
+ *   tgt_ids, tgt_probs [B, gamma+1, kt]: target ("clean") support per
+ *       position, ids strictly ascending in [0, V); probs fp32 >= 0 as given
+ *       (not renormalised); position gamma is the bonus list
+ *   drf_ids, drf_probs [B, gamma, kd]: draft support per position, same rules
+ *   draft_tokens [B, gamma] int32; u_accept [B, gamma]; u_sample [B]
+ * p_spec / q_spec are the listed probabilities at the draft token (0 when
+ * absent); after a rejection the draw is over the target list with weights
+ * max(p - q_on_clean, 0), q_on_clean being the draft probability of the same
+ * id; the bonus draw is over the target list of position gamma.
+ * Outputs: n_accepted [B]; out_tokens [B, gamma+1] (vocabulary ids);
+ *   residual_out [B, kt] fp32 or NULL (on the target support, list order);
+ *   accept_prob_out [B, gamma] fp32 or NULL.
+ * Limits: 1 <= kt, kd <= SV_MAX_LIST; gamma <= 31.
+ */
+int spec_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,
+                       const int32_t* drf_ids, const float* drf_probs, int kd,
+                       const int32_t* draft_tokens, const float* u_accept, const float* u_sample,
+                       int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                       float* residual_out, float* accept_prob_out, void* workspace,
+                       size_t ws_bytes, sv_stream_t stream);
+
+/*
+ * spec_verify_anyorder -- masked-diffusion self-speculative verification
+ * (Self-Speculative Masked Diffusions, key design 2).
+ *   target_logits, draft_logits [B, D, V] in sequence-position order
+ *   order        [B, W] int32: sigma, the W window positions (distinct, in
+ *                [0, D)) in verification order
+ *   draft_tokens [B, D] int32: the non-causal draft's token at each position
+ *   u_accept     [B, W] fp32 in window order; u_sample [B]
+ * Outputs: n_accepted [B] in [0, W] (-1: bad input); out_tokens [B, D]:
+ *   out[b, sigma_i] = draft token for i < n, the resample for i == n, -1 for
+ *   i > n; positions outside the window are not written.  No bonus token:
+ *   an all-accept round emits W tokens.  residual_out [B, V] or NULL (zeros
+ *   when n == W); accept_prob_out [B, W] or NULL.
+ * Limits: W <= 32, V <= 1024 (small-vocabulary kernel).
+ */
+int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                         const int32_t* order, const int32_t* draft_tokens,
+                         const float* u_accept, const float* u_sample, int B, int D, int W,
+                         int V, int32_t* n_accepted, int32_t* out_tokens, float* residual_out,
+                         float* accept_prob_out, void* workspace, size_t ws_bytes,
+                         sv_stream_t stream);
+
+/*
+ * spec_verify_check -- synchronise `stream`, read and clear the workspace
+ * status word.  Returns SV_OK, SV_ERR_DEVICE_INPUT (some row of an earlier
+ * call had invalid inputs; those rows carry n_accepted = -1),
+ * SV_ERR_TIMEOUT (a bounded wait ran out; re-initialise the workspace) or
+ * SV_ERR_CUDA.
+ */
+int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/* Static string for a status code. */
+const char* spec_verify_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPEC_VERIFY_H */

@@ -1,1 +1,23 @@
-"""GB300-native batched lossless speculative verification (binding filled in below)."""
+"""GB300-native batched lossless speculative verification.
+
+The verification step of drafter-and-verifier decoding (Leviathan-style
+rejection sampling) behind a C ABI (include/spec_verify.h) implemented by
+hand-written CUDA kernels for sm_103a in libspec_verify.so:
+
+  spec_verify_dense     dense logits, fused single-pass persistent kernel
+                        (small vocabularies: one warp per row)
+  spec_verify_sparse    Uno-style sorted top-k (id, prob) support lists
+  spec_verify_anyorder  masked-diffusion any-order window, small vocabulary
+
+The Python functions below have the same names as the C entry points and only
+marshal torch tensors; the library is loaded lazily on first use and every
+call fails loudly if it is missing.  ``workloads`` generates the seeded
+synthetic inputs.
+"""
+from ._binding import (  # noqa: F401
+    EXPORTED, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_TIMEOUT,
+    SV_ERR_UNSUPPORTED, SV_F32, SV_OK, SpecVerifyError, VerifyResult, abi_version, check,
+    debug_dense_ticket, get_workspace, library_path, load, spec_verify_anyorder, spec_verify_dense,
+    spec_verify_sparse, status_string, workspace_size,
+)
+from ._build import build  # noqa: F401

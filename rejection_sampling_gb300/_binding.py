@@ -1,0 +1,286 @@
+"""Thin ctypes binding of libspec_verify.so (declared in include/spec_verify.h).
+
+Argument marshalling only: shapes, dtypes and devices are checked, outputs and
+a per-stream workspace are allocated with torch, and raw device pointers go to
+the C ABI.  Every step of the verification runs in the library's CUDA
+kernels.  There is no CPU fallback: if the library cannot be loaded, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import NamedTuple, Optional
+
+import torch
+
+from . import _build
+
+SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT = range(6)
+SV_F32, SV_BF16 = 0, 1
+
+# Every function declared in include/spec_verify.h and include/spec_verify_debug.h.
+EXPORTED = (
+    "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
+    "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
+    "spec_verify_status_string", "sv_debug_dense_ticket",
+)
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(build_if_missing: bool = False):
+    """Load libspec_verify.so (raises if it is missing and not built here)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(
+                    f"{path} is missing: build it first (python -c 'import __graft_entry__ as g; g.build()')")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.spec_verify_abi_version.restype = I
+        lib.spec_verify_abi_version.argtypes = []
+        lib.spec_verify_workspace_size.restype = Z
+        lib.spec_verify_workspace_size.argtypes = [I, I, I]
+        lib.spec_verify_workspace_init.restype = I
+        lib.spec_verify_workspace_init.argtypes = [P, Z, P]
+        lib.spec_verify_dense.restype = I
+        lib.spec_verify_dense.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_verify_sparse.restype = I
+        lib.spec_verify_sparse.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_verify_anyorder.restype = I
+        lib.spec_verify_anyorder.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, P, P, P, P, Z, P]
+        lib.spec_verify_check.restype = I
+        lib.spec_verify_check.argtypes = [P, Z, P]
+        lib.spec_verify_status_string.restype = ctypes.c_char_p
+        lib.spec_verify_status_string.argtypes = [I]
+        lib.sv_debug_dense_ticket.restype = I
+        lib.sv_debug_dense_ticket.argtypes = [ctypes.c_longlong, ctypes.c_longlong, I, I, I, I,
+                                              ctypes.POINTER(ctypes.c_longlong)]
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().spec_verify_status_string(int(status)).decode()
+
+
+def abi_version() -> int:
+    return int(load().spec_verify_abi_version())
+
+
+def workspace_size(B: int, gamma_or_W: int, V: int) -> int:
+    return int(load().spec_verify_workspace_size(int(B), int(gamma_or_W), int(V)))
+
+
+# ---------------------------------------------------------------------------
+# workspace cache: one zero-initialised buffer per (device, stream)
+# ---------------------------------------------------------------------------
+_ws_cache: dict = {}
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream], device: torch.device) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return int(s.cuda_stream)
+
+
+def get_workspace(nbytes: int, device: torch.device, stream_ptr: int) -> torch.Tensor:
+    """A zeroed workspace of at least nbytes for calls on this stream.  The
+    library leaves it zeroed after every successful call, so it is reused."""
+    key = (device.index, stream_ptr)
+    ws = _ws_cache.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        rc = load().spec_verify_workspace_init(ws.data_ptr(), ws.numel(), stream_ptr)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, "spec_verify_workspace_init")
+        _ws_cache[key] = ws
+    return ws
+
+
+def check(device=None, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """spec_verify_check on the cached workspace of this stream (syncs)."""
+    device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    sp = _stream_ptr(stream, device)
+    ws = _ws_cache.get((device.index, sp))
+    if ws is None:
+        return SV_OK
+    return int(load().spec_verify_check(ws.data_ptr(), ws.numel(), sp))
+
+
+class VerifyResult(NamedTuple):
+    n_accepted: torch.Tensor
+    out_tokens: torch.Tensor
+    residual: Optional[torch.Tensor]
+    accept_prob: Optional[torch.Tensor]
+
+
+def _req(t: torch.Tensor, name: str, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _logit_dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def spec_verify_dense(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                      draft_ids: torch.Tensor, u_accept: torch.Tensor, u_sample: torch.Tensor,
+                      *, residual: bool = False, accept_prob: bool = False,
+                      out: Optional[VerifyResult] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """Dense verification.  target [B, g+1, V], draft [B, g, V] (bf16 or fp32,
+    CUDA), draft_ids [B, g] int32, u_accept [B, g] fp32, u_sample [B] fp32."""
+    lib = load()
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_dense needs CUDA tensors")
+    dt = _logit_dtype(target_logits)
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    _req(target_logits, "target_logits", target_logits.dtype, (B, G + 1, V), dev)
+    _req(draft_logits, "draft_logits", target_logits.dtype, (B, G, V), dev)
+    _req(draft_ids, "draft_ids", torch.int32, (B, G), dev)
+    _req(u_accept, "u_accept", torch.float32, (B, G), dev)
+    _req(u_sample, "u_sample", torch.float32, (B,), dev)
+    if out is None:
+        out = VerifyResult(
+            torch.empty(B, dtype=torch.int32, device=dev),
+            torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+            torch.empty(B, V, dtype=torch.float32, device=dev) if residual else None,
+            torch.empty(B, G, dtype=torch.float32, device=dev) if accept_prob else None)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, G, V), dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_dense(
+            _ptr(target_logits), _ptr(draft_logits) if G > 0 else None, dt, _ptr(draft_ids),
+            _ptr(u_accept), _ptr(u_sample), B, G, V, _ptr(out.n_accepted), _ptr(out.out_tokens),
+            _ptr(out.residual), _ptr(out.accept_prob), ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_dense")
+    return out
+
+
+def spec_verify_sparse(tgt_ids: torch.Tensor, tgt_probs: torch.Tensor, drf_ids: torch.Tensor,
+                       drf_probs: torch.Tensor, draft_tokens: torch.Tensor, u_accept: torch.Tensor,
+                       u_sample: torch.Tensor, vocab_size: int, *, residual: bool = False,
+                       accept_prob: bool = False, out: Optional[VerifyResult] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """Sparse top-k verification.  tgt_* [B, g+1, kt], drf_* [B, g, kd]; ids
+    int32 sorted ascending, probs fp32."""
+    lib = load()
+    dev = tgt_ids.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_sparse needs CUDA tensors")
+    B, G1, kt = tgt_ids.shape
+    G = G1 - 1
+    kd = drf_ids.shape[2] if drf_ids.dim() == 3 else 1
+    _req(tgt_ids, "tgt_ids", torch.int32, (B, G + 1, kt), dev)
+    _req(tgt_probs, "tgt_probs", torch.float32, (B, G + 1, kt), dev)
+    _req(drf_ids, "drf_ids", torch.int32, (B, G, kd), dev)
+    _req(drf_probs, "drf_probs", torch.float32, (B, G, kd), dev)
+    _req(draft_tokens, "draft_tokens", torch.int32, (B, G), dev)
+    _req(u_accept, "u_accept", torch.float32, (B, G), dev)
+    _req(u_sample, "u_sample", torch.float32, (B,), dev)
+    if out is None:
+        out = VerifyResult(
+            torch.empty(B, dtype=torch.int32, device=dev),
+            torch.empty(B, G + 1, dtype=torch.int32, device=dev),
+            torch.empty(B, kt, dtype=torch.float32, device=dev) if residual else None,
+            torch.empty(B, G, dtype=torch.float32, device=dev) if accept_prob else None)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_sparse(
+            _ptr(tgt_ids), _ptr(tgt_probs), kt, _ptr(drf_ids) if G else None,
+            _ptr(drf_probs) if G else None, kd, _ptr(draft_tokens) if G else None,
+            _ptr(u_accept) if G else None, _ptr(u_sample), B, G, int(vocab_size),
+            _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.residual), _ptr(out.accept_prob),
+            ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_sparse")
+    return out
+
+
+def spec_verify_anyorder(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                         order: torch.Tensor, draft_tokens: torch.Tensor, u_accept: torch.Tensor,
+                         u_sample: torch.Tensor, *, out_tokens: Optional[torch.Tensor] = None,
+                         residual: bool = False, accept_prob: bool = False,
+                         stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """Any-order verification.  target/draft [B, D, V], order [B, W] int32,
+    draft_tokens [B, D] int32, u_accept [B, W], u_sample [B].  out_tokens
+    [B, D] is updated in place at the window positions (allocated filled with
+    -1 if not given)."""
+    lib = load()
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_anyorder needs CUDA tensors")
+    dt = _logit_dtype(target_logits)
+    B, D, V = target_logits.shape
+    W = order.shape[1]
+    _req(target_logits, "target_logits", target_logits.dtype, (B, D, V), dev)
+    _req(draft_logits, "draft_logits", target_logits.dtype, (B, D, V), dev)
+    _req(order, "order", torch.int32, (B, W), dev)
+    _req(draft_tokens, "draft_tokens", torch.int32, (B, D), dev)
+    _req(u_accept, "u_accept", torch.float32, (B, W), dev)
+    _req(u_sample, "u_sample", torch.float32, (B,), dev)
+    if out_tokens is None:
+        out_tokens = torch.full((B, D), -1, dtype=torch.int32, device=dev)
+    _req(out_tokens, "out_tokens", torch.int32, (B, D), dev)
+    res = VerifyResult(
+        torch.empty(B, dtype=torch.int32, device=dev), out_tokens,
+        torch.empty(B, V, dtype=torch.float32, device=dev) if residual else None,
+        torch.empty(B, W, dtype=torch.float32, device=dev) if accept_prob else None)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_anyorder(
+            _ptr(target_logits), _ptr(draft_logits), dt, _ptr(order), _ptr(draft_tokens),
+            _ptr(u_accept), _ptr(u_sample), B, D, W, V, _ptr(res.n_accepted), _ptr(out_tokens),
+            _ptr(res.residual), _ptr(res.accept_prob), ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_anyorder")
+    return res
+
+
+def debug_dense_ticket(t: int, B: int, gamma: int, V: int, es: int, lag: int):
+    out = (ctypes.c_longlong * 3)()
+    rc = load().sv_debug_dense_ticket(int(t), int(B), int(gamma), int(V), int(es), int(lag), out)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "sv_debug_dense_ticket")
+    return int(out[0]), int(out[1]), int(out[2])

@@ -1,0 +1,278 @@
+// sv_api.cu -- host side of the C ABI declared in include/spec_verify.h:
+// argument validation, kernel selection, workspace layout, status word.
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/spec_verify.h"
+#include "sv_internal.h"
+
+namespace {
+
+constexpr long long kWaitBoundCycles = 4000000000LL;  // ~2 s at GB300 clocks
+
+int sm_count_for_current_device() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The small warp-per-row kernel handles R <= 32 rows per warp if the staged
+// block fits in 96 KB of shared memory.
+int small_vstride(int V) { return (V % 2) ? V : V + 1; }
+bool small_fits(int R, int V) {
+  return R >= 1 && R <= 32 && sv::small_smem_per_warp(R, small_vstride(V)) <= 96 * 1024;
+}
+
+size_t dense_ws_bytes(long long B, int G, int V, int es) {
+  const sv::DenseGeom g = sv::dense_geom(V, es);
+  return sv::dense_layout(B, G, g).total;
+}
+
+sv_status launch_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_abi_version(void) { return SV_ABI_VERSION; }
+
+size_t spec_verify_workspace_size(int B, int gamma_or_W, int V) {
+  if (B < 0 || gamma_or_W < 0 || V <= 0) return 0;
+  // fp32 rows need the most pieces, so they bound both dtypes
+  const size_t d = dense_ws_bytes(B, gamma_or_W, V, 4);
+  return d > sizeof(sv::WsHeader) ? d : sizeof(sv::WsHeader);
+}
+
+sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!workspace || ws_bytes < sizeof(sv::WsHeader)) return SV_ERR_INVALID_ARG;
+  return launch_status(cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream));
+}
+
+int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                      const int32_t* draft_ids, const float* u_accept, const float* u_sample,
+                      int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                      float* residual_out, float* accept_prob_out, void* workspace,
+                      size_t ws_bytes, sv_stream_t stream) {
+  if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !u_sample || !n_accepted || !out_tokens || !workspace) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && (!draft_logits || !draft_ids || !u_accept)) return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(target_logits, es) || (draft_logits && !aligned_to(draft_logits, es)))
+    return SV_ERR_INVALID_ARG;
+  if (!aligned_to(u_sample, 4) || !aligned_to(n_accepted, 4) || !aligned_to(out_tokens, 4) ||
+      (draft_ids && !aligned_to(draft_ids, 4)) || (u_accept && !aligned_to(u_accept, 4)) ||
+      (residual_out && !aligned_to(residual_out, 4)) ||
+      (accept_prob_out && !aligned_to(accept_prob_out, 4)) || !aligned_to(workspace, 256))
+    return SV_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(sv::WsHeader)) return SV_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  sv::WsHeader* hdr = reinterpret_cast<sv::WsHeader*>(workspace);
+
+  if (small_fits(gamma + 1, V)) {
+    sv::SmallParams p;
+    memset(&p, 0, sizeof p);
+    p.lt = static_cast<const unsigned char*>(target_logits);
+    p.ld = static_cast<const unsigned char*>(draft_logits);
+    p.x = draft_ids;
+    p.order = nullptr;
+    p.u_acc = u_accept;
+    p.u_s = u_sample;
+    p.n_out = n_accepted;
+    p.tok_out = out_tokens;
+    p.resid_out = residual_out;
+    p.acc_out = accept_prob_out;
+    p.status = &hdr->status;
+    p.B = B;
+    p.V = V;
+    p.R = gamma + 1;
+    p.G = gamma;
+    p.D = 0;
+    p.anyorder = 0;
+    p.bf16 = (dtype == SV_BF16);
+    p.vstride = small_vstride(V);
+    return launch_status(sv::launch_small(p, s));
+  }
+
+  const sv::DenseGeom g = sv::dense_geom(V, es);
+  const sv::DenseLayout L = sv::dense_layout(B, gamma, g);
+  if (ws_bytes < L.total) return SV_ERR_INVALID_ARG;
+  const int sms = sm_count_for_current_device();
+  if (sms <= 0) return SV_ERR_CUDA;
+  sv::DenseParams p;
+  memset(&p, 0, sizeof p);
+  p.lt = static_cast<const unsigned char*>(target_logits);
+  p.ld = static_cast<const unsigned char*>(draft_logits);
+  p.x = draft_ids;
+  p.u_acc = u_accept;
+  p.u_s = u_sample;
+  p.n_out = n_accepted;
+  p.tok_out = out_tokens;
+  p.acc_out = accept_prob_out;
+  p.ws = static_cast<unsigned char*>(workspace);
+  p.L = L;
+  p.g = g;
+  p.B = B;
+  p.G = gamma;
+  p.V = V;
+  p.bf16 = (dtype == SV_BF16);
+  p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(target_logits, 16) &&
+              (!draft_logits || aligned_to(draft_logits, 16));
+  const long long per_row = (long long)(gamma + 1) * g.nc_s + g.nc_r;
+  p.tickets = per_row * (long long)B;
+  long long grid = (long long)sms * sv::dense_ctas_per_sm();
+  if (grid > p.tickets) grid = p.tickets;
+  const long long units_per_row = (long long)(gamma + 1) * g.nc_s;
+  // residual units of row r wait for row r's statistics: schedule them after
+  // roughly two units per CTA of further statistics work
+  p.lag = (int)((2 * grid + units_per_row - 1) / units_per_row) + 1;
+  p.wait_bound = kWaitBoundCycles;
+  cudaError_t e = sv::launch_dense(p, (int)grid, s);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  if (residual_out) {
+    e = sv::launch_dense_resid_out(p, residual_out, s);
+    if (e != cudaSuccess) return SV_ERR_CUDA;
+  }
+  return SV_OK;
+}
+
+int spec_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,
+                       const int32_t* drf_ids, const float* drf_probs, int kd,
+                       const int32_t* draft_tokens, const float* u_accept, const float* u_sample,
+                       int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                       float* residual_out, float* accept_prob_out, void* workspace,
+                       size_t ws_bytes, sv_stream_t stream) {
+  if (B < 0 || gamma < 0 || gamma > 31 || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (kt < 1 || kt > SV_MAX_LIST || (gamma > 0 && (kd < 1 || kd > SV_MAX_LIST)))
+    return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!tgt_ids || !tgt_probs || !u_sample || !n_accepted || !out_tokens || !workspace)
+    return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && (!drf_ids || !drf_probs || !draft_tokens || !u_accept)) return SV_ERR_INVALID_ARG;
+  const void* ptrs[] = {tgt_ids, tgt_probs, drf_ids, drf_probs, draft_tokens, u_accept,
+                        u_sample, n_accepted, out_tokens, residual_out, accept_prob_out};
+  for (const void* q : ptrs)
+    if (q && !aligned_to(q, 4)) return SV_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(sv::WsHeader) || !aligned_to(workspace, 256)) return SV_ERR_INVALID_ARG;
+  sv::SparseParams p;
+  memset(&p, 0, sizeof p);
+  p.tid = tgt_ids;
+  p.tp = tgt_probs;
+  p.did = drf_ids;
+  p.dp = drf_probs;
+  p.x = draft_tokens;
+  p.u_acc = u_accept;
+  p.u_s = u_sample;
+  p.n_out = n_accepted;
+  p.tok_out = out_tokens;
+  p.resid_out = residual_out;
+  p.acc_out = accept_prob_out;
+  p.status = &reinterpret_cast<sv::WsHeader*>(workspace)->status;
+  p.B = B;
+  p.G = gamma;
+  p.V = V;
+  p.kt = kt;
+  p.kd = gamma > 0 ? kd : 1;
+  return launch_status(sv::launch_sparse(p, (cudaStream_t)stream));
+}
+
+int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                         const int32_t* order, const int32_t* draft_tokens,
+                         const float* u_accept, const float* u_sample, int B, int D, int W,
+                         int V, int32_t* n_accepted, int32_t* out_tokens, float* residual_out,
+                         float* accept_prob_out, void* workspace, size_t ws_bytes,
+                         sv_stream_t stream) {
+  if (B < 0 || W < 1 || W > 32 || D < W || D > SV_MAX_GAMMA * 64 || V < 1 || V > SV_MAX_VOCAB)
+    return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (!small_fits(W, V)) return SV_ERR_UNSUPPORTED;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !order || !draft_tokens || !u_accept || !u_sample ||
+      !n_accepted || !out_tokens || !workspace)
+    return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(target_logits, es) || !aligned_to(draft_logits, es)) return SV_ERR_INVALID_ARG;
+  const void* ptrs[] = {order, draft_tokens, u_accept, u_sample, n_accepted, out_tokens,
+                        residual_out, accept_prob_out};
+  for (const void* q : ptrs)
+    if (q && !aligned_to(q, 4)) return SV_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(sv::WsHeader) || !aligned_to(workspace, 256)) return SV_ERR_INVALID_ARG;
+  sv::SmallParams p;
+  memset(&p, 0, sizeof p);
+  p.lt = static_cast<const unsigned char*>(target_logits);
+  p.ld = static_cast<const unsigned char*>(draft_logits);
+  p.x = draft_tokens;
+  p.order = order;
+  p.u_acc = u_accept;
+  p.u_s = u_sample;
+  p.n_out = n_accepted;
+  p.tok_out = out_tokens;
+  p.resid_out = residual_out;
+  p.acc_out = accept_prob_out;
+  p.status = &reinterpret_cast<sv::WsHeader*>(workspace)->status;
+  p.B = B;
+  p.V = V;
+  p.R = W;
+  p.G = W;
+  p.D = D;
+  p.anyorder = 1;
+  p.bf16 = (dtype == SV_BF16);
+  p.vstride = small_vstride(V);
+  return launch_status(sv::launch_small(p, (cudaStream_t)stream));
+}
+
+int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!workspace || ws_bytes < sizeof(sv::WsHeader)) return SV_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  sv::WsHeader h;
+  if (cudaMemcpyAsync(&h, workspace, sizeof h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return SV_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  if (h.status) {
+    // clear status and abort (two adjacent words)
+    sv::WsHeader* d = reinterpret_cast<sv::WsHeader*>(workspace);
+    if (cudaMemsetAsync(&d->status, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  }
+  if (h.status & sv::kStatusTimeout) return SV_ERR_TIMEOUT;
+  if (h.status & sv::kStatusInputErr) return SV_ERR_DEVICE_INPUT;
+  return SV_OK;
+}
+
+const char* spec_verify_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_INVALID_ARG: return "invalid argument";
+    case SV_ERR_UNSUPPORTED: return "unsupported request";
+    case SV_ERR_CUDA: return "CUDA error";
+    case SV_ERR_DEVICE_INPUT: return "invalid input rows (n_accepted = -1)";
+    case SV_ERR_TIMEOUT: return "bounded device wait expired; re-initialise the workspace";
+    default: return "unknown status";
+  }
+}
+
+// Host-side view of the dense kernel's ticket order, for tests of the
+// schedule: fills out[0] = is_residual, out[1] = row, out[2] = remainder.
+int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, int lag,
+                          long long* out3) {
+  if (!out3 || (es != 2 && es != 4) || B <= 0 || gamma < 0 || V <= 0 || lag < 1) return SV_ERR_INVALID_ARG;
+  const sv::DenseGeom g = sv::dense_geom(V, es);
+  int resid = 0, b = 0;
+  long long rem = 0;
+  sv::dense_ticket_row(t, B, gamma, g.nc_s, g.nc_r, lag, &resid, &b, &rem);
+  out3[0] = resid;
+  out3[1] = b;
+  out3[2] = rem;
+  return SV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,236 @@
+// sv_small.cu -- warp-per-row verification for small vocabularies.
+//
+// One warp verifies one row (dense) or one sequence window (any-order).  The
+// row block is staged in shared memory with an odd row stride, so lane i can
+// read position i's row with no bank conflicts; lane i owns position i:
+// softmax statistics of its target and draft rows, the gather at its draft
+// token and its accept test.  A ballot gives the first rejection; the whole
+// warp then draws the replacement (or the bonus token) by an fp64 prefix over
+// the fp32 residual values in ascending id order.
+//
+//  dense     : positions 0..gamma; target rows 0..gamma, draft rows 0..gamma-1;
+//              bonus from p_gamma when every draft is accepted (DFlash/DFlash2
+//              guide, section 2).
+//  any-order : window index i verifies sequence position sigma_i; the round
+//              ends at the first rejection, whose position is resampled from
+//              max(0, target - draft); no bonus (Self-Speculative Masked
+//              Diffusions, key design 2).
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+__device__ __forceinline__ float ld_logit(const unsigned char* base, size_t idx, int bf16) {
+  if (bf16) return bf16_to_f32(reinterpret_cast<const uint16_t*>(base)[idx]);
+  return reinterpret_cast<const float*>(base)[idx];
+}
+
+__device__ __forceinline__ float resid_val(float t, float d, float ct, float cd, float invSt,
+                                           float invSd, int mode) {
+  const float p = __fmul_rn(ex2(__fmaf_rn(t, kLog2e, -ct)), invSt);
+  if (mode != 0) return p;
+  const float q = __fmul_rn(ex2(__fmaf_rn(d, kLog2e, -cd)), invSd);
+  const float r = __fsub_rn(p, q);
+  return r > 0.f ? r : 0.f;
+}
+
+// softmax statistics of one shared-memory row: c = log2e * max, S = sum 2^(v log2e - c)
+__device__ __forceinline__ void row_stats(const float* row, int V, float& c_out, float& s_out) {
+  float m = -INFINITY;
+  for (int y = 0; y < V; ++y) m = fmaxf(m, row[y]);
+  const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int y = 0;
+  for (; y + 3 < V; y += 4) {
+    a0 += ex2(fmaf(row[y], kLog2e, -c));
+    a1 += ex2(fmaf(row[y + 1], kLog2e, -c));
+    a2 += ex2(fmaf(row[y + 2], kLog2e, -c));
+    a3 += ex2(fmaf(row[y + 3], kLog2e, -c));
+  }
+  for (; y < V; ++y) a0 += ex2(fmaf(row[y], kLog2e, -c));
+  s_out = (a0 + a1) + (a2 + a3);
+  c_out = (m == -INFINITY) ? -INFINITY : c;
+}
+
+__device__ __forceinline__ bool stats_ok(float c, float s) {
+  return c > -INFINITY && c < INFINITY && s > 0.f && s < INFINITY;
+}
+
+__global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
+  extern __shared__ float smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + warp;
+  if (b >= P.B) return;  // whole warp leaves; no block-wide barrier below
+  const int R = P.R, VS = P.vstride, V = P.V, NT = P.G;  // NT accept tests
+  float* st = smem + (size_t)warp * 2 * R * VS;
+  float* sd = st + (size_t)R * VS;
+
+  // ---- rows and validation of the window ----
+  int sig = lane, bad = 0;
+  if (P.anyorder) {
+    if (lane < R) {
+      sig = P.order[(size_t)b * R + lane];
+      if (sig < 0 || sig >= P.D) bad = 1;
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, lane < R ? sig : -1 - lane);
+    if (lane < R && __popc(same) > 1) bad = 1;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+
+  // ---- stage the rows in shared memory (row r of the warp = position r) ----
+  for (int r = 0; r < R; ++r) {
+    size_t trow, drow;
+    bool hasd;
+    if (P.anyorder) {
+      int s = __shfl_sync(0xffffffffu, sig, r);
+      if (bad) s = 0;
+      trow = drow = (size_t)b * P.D + s;
+      hasd = true;
+    } else {
+      trow = (size_t)b * (NT + 1) + r;
+      drow = (size_t)b * NT + r;
+      hasd = r < NT;
+    }
+    for (int y = lane; y < V; y += 32) {
+      st[r * VS + y] = ld_logit(P.lt, trow * V + y, P.bf16);
+      if (hasd) sd[r * VS + y] = ld_logit(P.ld, drow * V + y, P.bf16);
+    }
+  }
+  __syncwarp();
+
+  // ---- per-position statistics and accept test (lane = position) ----
+  float ct = 0.f, St = 1.f, cd = 0.f, Sd = 1.f, a = 0.f;
+  int err = bad, acc = 1, x = 0;
+  if (!bad && lane < R) {
+    row_stats(st + lane * VS, V, ct, St);
+    err |= !stats_ok(ct, St);
+    if (lane < NT) {
+      row_stats(sd + lane * VS, V, cd, Sd);
+      err |= !stats_ok(cd, Sd);
+      x = P.anyorder ? P.x[(size_t)b * P.D + sig] : P.x[(size_t)b * NT + lane];
+      if (x < 0 || x >= V) err = 1;
+      if (!err) {
+        const float tx = st[lane * VS + x], dx = sd[lane * VS + x];
+        float ratio = 0.f;
+        if (tx > -INFINITY && dx > -INFINITY) {
+          // log2 p(x) - log2 q(x) in fp64 (exact products), then one fp32 exp2
+          const double L = (double)kLog2e;
+          const double dl = ((double)tx * L - (double)ct) - ((double)dx * L - (double)cd);
+          ratio = exp2f((float)dl) * (Sd / St);
+        }
+        a = fminf(ratio, 1.f);
+        acc = P.u_acc[(size_t)b * NT + lane] < a;
+      }
+    }
+  }
+  err = __any_sync(0xffffffffu, err);
+  if (P.acc_out && lane < NT) P.acc_out[(size_t)b * NT + lane] = err ? __int_as_float(0x7fc00000) : a;
+  const unsigned rej = __ballot_sync(0xffffffffu, lane < NT && !acc);
+  const int n = err ? -1 : (rej ? __ffs(rej) - 1 : NT);
+
+  // ---- draw at the stop position ----
+  int y = -1;
+  int mode = 2;  // 0 residual, 1 p only, 2 none
+  double T = 0.0;
+  float sct = 0.f, scd = 0.f, sist = 0.f, sisd = 0.f;
+  int srow = 0;
+  if (n >= 0 && (n < NT || !P.anyorder)) {
+    mode = (n < NT) ? 0 : 1;
+    srow = n;  // shared-memory row of the stop position
+    sct = __shfl_sync(0xffffffffu, ct, n);
+    scd = __shfl_sync(0xffffffffu, cd, n);
+    sist = 1.f / __shfl_sync(0xffffffffu, St, n);
+    sisd = 1.f / __shfl_sync(0xffffffffu, Sd, n);
+    const int q = (V + 31) / 32;
+    const int e0 = min(V, lane * q), e1 = min(V, e0 + q);
+    const float* tr = st + srow * VS;
+    const float* dr = sd + srow * VS;
+    for (int attempt = 0; attempt < 2; ++attempt) {
+      double ls = 0.0;
+      for (int e = e0; e < e1; ++e) ls += (double)resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode);
+      const double ex = warp_exclusive_scan_d(ls, lane);
+      T = __shfl_sync(0xffffffffu, ex + ls, 31);
+      if (!(T > 0.0) && mode == 0) {  // zero residual through rounding: draw from p_n
+        mode = 1;
+        continue;
+      }
+      const double target = (double)P.u_s[b] * T;
+      const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && (ex + ls > target));
+      if (hit) {
+        const int fl = __ffs(hit) - 1;
+        if (lane == fl) {
+          double accm = ex;
+          int lastpos = -1;
+          for (int e = e0; e < e1; ++e) {
+            const float r = resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode);
+            if (r > 0.f) lastpos = e;
+            accm += (double)r;
+            if (accm > target) {
+              y = e;
+              break;
+            }
+          }
+          if (y < 0) y = lastpos >= 0 ? lastpos : e1 - 1;
+        }
+        y = __shfl_sync(0xffffffffu, y, fl);
+      } else {  // u*T at or past the total through rounding: last id with mass
+        int lp = -1;
+        for (int e = e0; e < e1; ++e)
+          if (resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode) > 0.f) lp = e;
+        for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+        y = lp < 0 ? 0 : lp;
+      }
+      break;
+    }
+  }
+
+  // ---- outputs ----
+  if (lane == 0) {
+    P.n_out[b] = n;
+    if (err) atomicOr(P.status, kStatusInputErr);
+  }
+  if (P.anyorder) {
+    if (lane < R && sig >= 0 && sig < P.D) {
+      int v = -1;
+      if (n >= 0) v = (lane < n) ? x : (lane == n ? y : -1);
+      P.tok_out[(size_t)b * P.D + sig] = v;
+    }
+  } else {
+    for (int j = lane; j <= NT; j += 32) {
+      int v = -1;
+      if (n >= 0) v = (j < n) ? P.x[(size_t)b * NT + j] : (j == n ? y : -1);
+      P.tok_out[(size_t)b * (NT + 1) + j] = v;
+    }
+  }
+  if (P.resid_out) {
+    float* o = P.resid_out + (size_t)b * V;
+    const bool have = (mode != 2) && (T > 0.0);
+    const double invT = have ? 1.0 / T : 0.0;
+    const float* tr = st + srow * VS;
+    const float* dr = sd + srow * VS;
+    for (int e = lane; e < V; e += 32)
+      o[e] = have ? (float)((double)resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode) * invT) : 0.f;
+  }
+}
+
+}  // namespace
+
+size_t small_smem_per_warp(int R, int vstride) { return (size_t)2 * R * vstride * sizeof(float); }
+
+cudaError_t launch_small(const SmallParams& p, cudaStream_t s) {
+  const size_t per = small_smem_per_warp(p.R, p.vstride);
+  int warps = (int)((96 * 1024) / per);
+  if (warps > 8) warps = 8;
+  if (warps < 1) warps = 1;
+  const size_t smem = per * warps;
+  if (smem > 48 * 1024) {
+    cudaError_t e =
+        cudaFuncSetAttribute(small_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  const long long blocks = ((long long)p.B + warps - 1) / warps;
+  small_verify_kernel<<<(unsigned)blocks, warps * 32, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sv

@@ -1,0 +1,179 @@
+// sv_sparse.cu -- verification on sorted top-k (id, prob) support lists.
+//
+// The rule as Uno's sampler states it (Uno article, "What 'lossless'
+// actually has to mean", _sparse_verify_tensors): p_spec and q_spec are the
+// listed probabilities at the draft token (0 where the id is absent), ratio =
+// p_spec / q_spec where q_spec > 0 else 0, accept iff u < min(1, ratio); the
+// correction after a rejection is clamp(p - q_on_clean, 0) on the target
+// ("clean") support, renormalised, q_on_clean being the draft probability of
+// the same id.  The block is truncated at the first rejection (DFlash/DFlash2
+// guide, 4.4) and an all-accept block draws the bonus from the target list of
+// position gamma (same guide, section 2).
+//
+// One CTA per row, one warp per position (gamma + 1 <= 32 warps).  Warp j
+// validates its lists and runs its accept test; a shared-memory scan finds
+// the first rejection n; warp n then merges its target list against the
+// sorted draft list (binary search per target id), scans the residual in fp64
+// in list order and draws the token.
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+__device__ __forceinline__ bool list_ok(const int32_t* ids, const float* pr, int k, int V,
+                                        int lane) {
+  bool ok = true;
+  for (int i = lane; i < k; i += 32) {
+    const int id = ids[i];
+    if (id < 0 || id >= V) ok = false;
+    if (i + 1 < k && ids[i + 1] <= id) ok = false;
+    const float p = pr[i];
+    if (!(p >= 0.f) || p == INFINITY) ok = false;
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
+// probability of `id` in a sorted list (0 if absent)
+__device__ __forceinline__ float list_lookup(const int32_t* ids, const float* pr, int k, int id) {
+  int lo = 0, hi = k;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    const int v = __ldg(ids + mid);
+    if (v < id)
+      lo = mid + 1;
+    else
+      hi = mid;
+  }
+  return (lo < k && __ldg(ids + lo) == id) ? __ldg(pr + lo) : 0.f;
+}
+
+__global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
+  __shared__ int s_acc[32];
+  __shared__ int s_err[32];
+  __shared__ int s_n;
+  const int b = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = P.G, kt = P.kt, kd = P.kd, V = P.V;
+  const int32_t* tid = P.tid + ((size_t)b * (G + 1) + j) * kt;
+  const float* tp = P.tp + ((size_t)b * (G + 1) + j) * kt;
+
+  bool err = !list_ok(tid, tp, kt, V, lane);
+  int acc = 1;
+  float a = 0.f;
+  if (j < G) {
+    const int32_t* did = P.did + ((size_t)b * G + j) * kd;
+    const float* dp = P.dp + ((size_t)b * G + j) * kd;
+    err |= !list_ok(did, dp, kd, V, lane);
+    const int x = P.x[(size_t)b * G + j];
+    if (x < 0 || x >= V) err = true;
+    float ps = 0.f, qs = 0.f;
+    for (int i = lane; i < kt; i += 32)
+      if (tid[i] == x) ps += tp[i];
+    for (int i = lane; i < kd; i += 32)
+      if (did[i] == x) qs += dp[i];
+    ps = warp_sum(ps);
+    qs = warp_sum(qs);
+    const float ratio = (qs > 0.f) ? __fdiv_rn(ps, qs) : 0.f;
+    a = fminf(ratio, 1.f);
+    acc = P.u_acc[(size_t)b * G + j] < a;
+  }
+  if (lane == 0) {
+    s_acc[j] = acc;
+    s_err[j] = err ? 1 : 0;
+    if (P.acc_out && j < G) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
+  }
+  __syncthreads();
+  if (j == 0) {
+    const int e = (lane <= G) ? s_err[lane] : 0;
+    const int r = (lane < G) ? !s_acc[lane] : 0;
+    const bool any_err = __any_sync(0xffffffffu, e);
+    const unsigned rej = __ballot_sync(0xffffffffu, r);
+    if (lane == 0) s_n = any_err ? -1 : (rej ? __ffs(rej) - 1 : G);
+  }
+  __syncthreads();
+  const int n = s_n;
+  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
+  if (n < 0) {
+    if (j == 0) {
+      for (int i = lane; i <= G; i += 32) tok[i] = -1;
+      if (lane == 0) {
+        P.n_out[b] = -1;
+        atomicOr(P.status, kStatusInputErr);
+      }
+      if (P.resid_out)
+        for (int i = lane; i < kt; i += 32) P.resid_out[(size_t)b * kt + i] = 0.f;
+    }
+    return;
+  }
+  if (j != n) return;
+
+  // ---- warp n: residual on the target support (or the bonus list) ----
+  const int32_t* did = (n < G) ? P.did + ((size_t)b * G + n) * kd : nullptr;
+  const float* dp = (n < G) ? P.dp + ((size_t)b * G + n) * kd : nullptr;
+  const int q = (kt + 31) / 32;
+  const int e0 = min(kt, lane * q), e1 = min(kt, e0 + q);
+  int mode = (n < G) ? 0 : 1;
+  auto weight = [&](int i) -> float {
+    const float p = tp[i];
+    if (mode != 0) return p;
+    const float r = __fsub_rn(p, list_lookup(did, dp, kd, tid[i]));
+    return r > 0.f ? r : 0.f;
+  };
+  double T = 0.0, ls = 0.0, ex = 0.0;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    ls = 0.0;
+    for (int i = e0; i < e1; ++i) ls += (double)weight(i);
+    ex = warp_exclusive_scan_d(ls, lane);
+    T = __shfl_sync(0xffffffffu, ex + ls, 31);
+    if (!(T > 0.0) && mode == 0) {
+      mode = 1;  // zero residual through rounding: draw from the target list
+      continue;
+    }
+    break;
+  }
+  int yi = -1;
+  if (T > 0.0) {
+    const double target = (double)P.u_s[b] * T;
+    const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && (ex + ls > target));
+    if (hit) {
+      const int fl = __ffs(hit) - 1;
+      if (lane == fl) {
+        double accm = ex;
+        int lastpos = -1;
+        for (int i = e0; i < e1; ++i) {
+          const float w = weight(i);
+          if (w > 0.f) lastpos = i;
+          accm += (double)w;
+          if (accm > target) {
+            yi = i;
+            break;
+          }
+        }
+        if (yi < 0) yi = lastpos >= 0 ? lastpos : e1 - 1;
+      }
+      yi = __shfl_sync(0xffffffffu, yi, fl);
+    } else {
+      int lp = -1;
+      for (int i = e0; i < e1; ++i)
+        if (weight(i) > 0.f) lp = i;
+      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+      yi = lp;
+    }
+  }
+  const int y = (yi >= 0) ? tid[yi] : -1;
+  for (int i = lane; i <= G; i += 32) tok[i] = (i < n) ? P.x[(size_t)b * G + i] : (i == n ? y : -1);
+  if (lane == 0) P.n_out[b] = n;
+  if (P.resid_out) {
+    const double invT = (T > 0.0) ? 1.0 / T : 0.0;
+    for (int i = lane; i < kt; i += 32)
+      P.resid_out[(size_t)b * kt + i] = (float)((double)weight(i) * invT);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
+  sparse_verify_kernel<<<p.B, 32 * (p.G + 1), 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace sv
