@@ -86,9 +86,10 @@ int spec_verify_abi_version(void);
  * enough for any of the three calls with those sizes (B rows, gamma drafts
  * or a window of W, vocabulary V).  The workspace must be zeroed once before
  * first use -- spec_verify_workspace_init() does that on `stream` -- and each
- * successful call leaves its counters at zero again, so a call can be
- * replayed (e.g. from a CUDA graph) without re-initialising.  One workspace
- * must not be used by two calls that may run at the same time.
+ * successful call leaves every byte of it (apart from the sticky status word)
+ * at zero again, so one workspace serves calls of any sizes that fit it, and
+ * a call can be replayed (e.g. from a CUDA graph) without re-initialising.
+ * One workspace must not be used by two calls that may run at the same time.
  */
 size_t spec_verify_workspace_size(int B, int gamma_or_W, int V);
 sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream);

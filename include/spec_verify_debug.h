@@ -10,15 +10,14 @@ extern "C" {
 #endif
 
 /*
- * Work order of the dense persistent kernel.  For ticket t of a call with B
- * rows, gamma drafts, vocabulary V, element size es (2 or 4 bytes) and a lag
- * of `lag` rows between a row's statistics units and its residual units,
- * writes out3[0] = 1 for a residual unit (0 for statistics), out3[1] = the
- * row, out3[2] = the unit's index among that row's units of that kind.
- * Returns 0, or SV_ERR_INVALID_ARG (1) for bad arguments.
+ * Statistics work order of the dense persistent kernel.  For ticket t of a
+ * call with B rows, gamma drafts, vocabulary V and element size es (2 or 4
+ * bytes), writes out3 = (row, position, unit within the position).
+ * Returns 0; SV_ERR_INVALID_ARG (1) for bad arguments or t out of range;
+ * SV_ERR_UNSUPPORTED (2) if the kernel's 32-bit decode of t disagrees with
+ * plain 64-bit division.
  */
-int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, int lag,
-                          long long* out3);
+int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, long long* out3);
 
 #ifdef __cplusplus
 }

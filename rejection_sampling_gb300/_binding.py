@@ -73,7 +73,7 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.spec_verify_status_string.argtypes = [I]
         lib.sv_debug_dense_ticket.restype = I
-        lib.sv_debug_dense_ticket.argtypes = [ctypes.c_longlong, ctypes.c_longlong, I, I, I, I,
+        lib.sv_debug_dense_ticket.argtypes = [ctypes.c_longlong, ctypes.c_longlong, I, I, I,
                                               ctypes.POINTER(ctypes.c_longlong)]
         _lib = lib
         return lib
@@ -118,7 +118,10 @@ def get_workspace(nbytes: int, device: torch.device, stream_ptr: int) -> torch.T
 
 def check(device=None, stream: Optional[torch.cuda.Stream] = None) -> int:
     """spec_verify_check on the cached workspace of this stream (syncs)."""
-    device = torch.device("cuda", torch.cuda.current_device() if device is None else device)
+    if device is None:
+        device = torch.device("cuda", torch.cuda.current_device())
+    elif not isinstance(device, torch.device):
+        device = torch.device("cuda", int(device))
     sp = _stream_ptr(stream, device)
     ws = _ws_cache.get((device.index, sp))
     if ws is None:
@@ -278,9 +281,81 @@ def spec_verify_anyorder(target_logits: torch.Tensor, draft_logits: torch.Tensor
     return res
 
 
-def debug_dense_ticket(t: int, B: int, gamma: int, V: int, es: int, lag: int):
+def debug_dense_ticket(t: int, B: int, gamma: int, V: int, es: int):
+    """(row, position, unit) of statistics ticket t of the dense kernel."""
     out = (ctypes.c_longlong * 3)()
-    rc = load().sv_debug_dense_ticket(int(t), int(B), int(gamma), int(V), int(es), int(lag), out)
+    rc = load().sv_debug_dense_ticket(int(t), int(B), int(gamma), int(V), int(es), out)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "sv_debug_dense_ticket")
     return int(out[0]), int(out[1]), int(out[2])
+
+
+class PreparedCall:
+    """A C-ABI call with every argument marshalled once.  Calling it issues
+    exactly one library call (no tensor allocation, no checks) on the stream
+    it was prepared for; the caller keeps the tensors alive."""
+
+    def __init__(self, fn, args, keep, name):
+        self._fn, self._args, self._keep, self.name = fn, args, keep, name
+
+    def __call__(self) -> None:
+        rc = self._fn(*self._args)
+        if rc != SV_OK:
+            raise SpecVerifyError(rc, self.name)
+
+
+def prepare_dense(target_logits, draft_logits, draft_ids, u_accept, u_sample, out: VerifyResult,
+                  stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """Validate once (by running the checked call) and return a PreparedCall
+    that repeats spec_verify_dense on the same buffers."""
+    spec_verify_dense(target_logits, draft_logits, draft_ids, u_accept, u_sample, out=out,
+                      stream=stream)
+    lib = load()
+    dev = target_logits.device
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, G, V), dev, sp)
+    args = (_ptr(target_logits), _ptr(draft_logits) if G > 0 else None,
+            _logit_dtype(target_logits), _ptr(draft_ids), _ptr(u_accept), _ptr(u_sample), B, G, V,
+            _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.residual), _ptr(out.accept_prob),
+            ws.data_ptr(), ws.numel(), sp)
+    keep = (target_logits, draft_logits, draft_ids, u_accept, u_sample, out, ws)
+    return PreparedCall(lib.spec_verify_dense, args, keep, "spec_verify_dense")
+
+
+def prepare_sparse(tgt_ids, tgt_probs, drf_ids, drf_probs, draft_tokens, u_accept, u_sample,
+                   vocab_size, out: VerifyResult, stream=None) -> PreparedCall:
+    spec_verify_sparse(tgt_ids, tgt_probs, drf_ids, drf_probs, draft_tokens, u_accept, u_sample,
+                       vocab_size, out=out, stream=stream)
+    lib = load()
+    dev = tgt_ids.device
+    B, G1, kt = tgt_ids.shape
+    G = G1 - 1
+    kd = drf_ids.shape[2] if drf_ids.dim() == 3 else 1
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    args = (_ptr(tgt_ids), _ptr(tgt_probs), kt, _ptr(drf_ids) if G else None,
+            _ptr(drf_probs) if G else None, kd, _ptr(draft_tokens) if G else None,
+            _ptr(u_accept) if G else None, _ptr(u_sample), B, G, int(vocab_size),
+            _ptr(out.n_accepted), _ptr(out.out_tokens), _ptr(out.residual), _ptr(out.accept_prob),
+            ws.data_ptr(), ws.numel(), sp)
+    keep = (tgt_ids, tgt_probs, drf_ids, drf_probs, draft_tokens, u_accept, u_sample, out, ws)
+    return PreparedCall(lib.spec_verify_sparse, args, keep, "spec_verify_sparse")
+
+
+def prepare_anyorder(target_logits, draft_logits, order, draft_tokens, u_accept, u_sample,
+                     out_tokens, stream=None) -> PreparedCall:
+    res = spec_verify_anyorder(target_logits, draft_logits, order, draft_tokens, u_accept, u_sample,
+                               out_tokens=out_tokens, stream=stream)
+    lib = load()
+    dev = target_logits.device
+    B, D, V = target_logits.shape
+    W = order.shape[1]
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    args = (_ptr(target_logits), _ptr(draft_logits), _logit_dtype(target_logits), _ptr(order),
+            _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample), B, D, W, V, _ptr(res.n_accepted),
+            _ptr(out_tokens), None, None, ws.data_ptr(), ws.numel(), sp)
+    keep = (target_logits, draft_logits, order, draft_tokens, u_accept, u_sample, out_tokens, res, ws)
+    return PreparedCall(lib.spec_verify_anyorder, args, keep, "spec_verify_anyorder")

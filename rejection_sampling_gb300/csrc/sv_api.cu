@@ -127,15 +127,15 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
   p.bf16 = (dtype == SV_BF16);
   p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(target_logits, 16) &&
               (!draft_logits || aligned_to(draft_logits, 16));
-  const long long per_row = (long long)(gamma + 1) * g.nc_s + g.nc_r;
-  p.tickets = per_row * (long long)B;
+  p.tickets = (long long)(gamma + 1) * g.nc_s * (long long)B;
+  if ((long long)g.nc_r * B >= (1ll << 31) - 65536) return SV_ERR_INVALID_ARG;
+  p.resid_units = (unsigned)((long long)g.nc_r * B);
+  p.small_tickets = (p.tickets + 4 * 65536 < (1ll << 31)) ? 1 : 0;
   long long grid = (long long)sms * sv::dense_ctas_per_sm();
   if (grid > p.tickets) grid = p.tickets;
-  const long long units_per_row = (long long)(gamma + 1) * g.nc_s;
-  // residual units of row r wait for row r's statistics: schedule them after
-  // roughly two units per CTA of further statistics work
-  p.lag = (int)((2 * grid + units_per_row - 1) / units_per_row) + 1;
   p.wait_bound = kWaitBoundCycles;
+  p.keep_stop = residual_out != nullptr;
+  p.tk = sv::make_ticket_consts(gamma, g.nc_s);
   cudaError_t e = sv::launch_dense(p, (int)grid, s);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   if (residual_out) {
@@ -260,18 +260,24 @@ const char* spec_verify_status_string(int status) {
   }
 }
 
-// Host-side view of the dense kernel's ticket order, for tests of the
-// schedule: fills out[0] = is_residual, out[1] = row, out[2] = remainder.
-int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, int lag,
-                          long long* out3) {
-  if (!out3 || (es != 2 && es != 4) || B <= 0 || gamma < 0 || V <= 0 || lag < 1) return SV_ERR_INVALID_ARG;
+// Host-side view of the dense kernel's statistics ticket order, for tests:
+// out3 = (row, position, unit) of ticket t.
+int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, long long* out3) {
+  if (!out3 || (es != 2 && es != 4) || B <= 0 || gamma < 0 || V <= 0) return SV_ERR_INVALID_ARG;
   const sv::DenseGeom g = sv::dense_geom(V, es);
-  int resid = 0, b = 0;
-  long long rem = 0;
-  sv::dense_ticket_row(t, B, gamma, g.nc_s, g.nc_r, lag, &resid, &b, &rem);
-  out3[0] = resid;
-  out3[1] = b;
-  out3[2] = rem;
+  if (t < 0 || t >= (long long)(gamma + 1) * g.nc_s * B) return SV_ERR_INVALID_ARG;
+  int b = 0, j = 0, c = 0;
+  sv::dense_ticket(t, gamma, g.nc_s, &b, &j, &c);
+  out3[0] = b;
+  out3[1] = j;
+  out3[2] = c;
+  // the 32-bit decode the kernel uses must agree with plain division
+  if (t < (1ll << 31)) {
+    const sv::TicketConsts k = sv::make_ticket_consts(gamma, g.nc_s);
+    int b2 = 0, j2 = 0, c2 = 0;
+    sv::dense_ticket_fast((unsigned)t, k, &b2, &j2, &c2);
+    if (b2 != b || j2 != j || c2 != c) return SV_ERR_UNSUPPORTED;
+  }
   return SV_OK;
 }
 

@@ -9,25 +9,28 @@
 //   (bonus, DFlash/DFlash2 guide section 2) at u_sample[b].
 //
 // Design (one persistent kernel, one launch per call):
-//  * Work is a stream of tickets taken with one atomicAdd each.  Tickets are
-//    ordered row by row: the statistics units of row r, then the residual
-//    units of row r - lag.  A statistics unit is up to 8 x 4 KB pieces of the
-//    target row (b, j) plus the same pieces of the draft row (b, j); a
-//    residual unit is up to 8 pieces of 2 KB target + 2 KB draft of the stop
-//    position (b, n).
-//  * Each CTA = 1 producer warp + 16 consumer warps around a 32-stage ring of
+//  * Statistics work is a stream of tickets in row order, taken with one
+//    atomicAdd each (prefetched one ahead).  A statistics unit is up to
+//    8 x 4 KB pieces of the target row (b, j) plus the same pieces of the
+//    draft row (b, j).  When a row's statistics are complete its finaliser
+//    publishes the row's residual units -- up to 8 pieces of 2 KB target +
+//    2 KB draft of the stop position (b, n) -- to a queue that producers
+//    drain before taking new tickets.
+//  * Each CTA = 1 producer warp + NW consumer warps around an NS-stage ring of
 //    4 KB shared-memory stages.  The producer moves pieces with 1-D bulk
-//    copies (cp.async.bulk, TMA) completing on per-stage mbarriers; every
-//    consumer warp takes every 16th stage.
+//    copies (cp.async.bulk, TMA) completing on per-stage mbarriers; consumer
+//    warp w takes stages w, w + NW, ...  A consumer releases its stage as soon
+//    as the data is in registers, so slow bookkeeping never holds the ring.
 //  * A consumer warp reduces a 4 KB piece to (c, s): c = log2e * max, s =
 //    sum 2^(v*log2e - c) (MUFU ex2).  The last warp of a unit combines the
-//    unit's pieces and publishes one partial; the last unit of a (row,
-//    position) finalises its accept test in fp64; the last position of a row
-//    finds the first rejection n and publishes the stop constants.  These
+//    unit's pieces and publishes one partial; the last unit of a row runs all
+//    of the row's accept tests (one lane per position, fp64), finds the first
+//    rejection n and publishes the stop constants.  These
 //    hand-offs are last-arriver atomics: no warp ever waits for another CTA
-//    except the producer of a residual unit, which waits (bounded) for its
-//    row's stop constants.  Every ticket it could wait on was taken earlier by
-//    a running CTA, so the wait always ends.
+//    while it holds statistics work.  A producer waits (bounded) for a queue
+//    entry only once every statistics ticket is taken; every such entry is
+//    published by a row whose statistics units are all held by running CTAs
+//    that never wait, so the wait always ends.
 //  * Residual units recompute r(y) = max(p(y) - q(y), 0) for the stop
 //    position only (the rows are still in L2: they were read a few rows of
 //    work earlier) and publish per-piece masses; the last one selects the
@@ -36,10 +39,6 @@
 
 namespace sv {
 namespace {
-
-constexpr int kNS = 32;  // ring stages
-constexpr int kNW = 16;  // consumer warps
-constexpr int kThreads = 32 * (kNW + 1);
 
 enum StageKind : int { kStatsT = 0, kStatsD = 1, kResid = 2, kResidSkip = 3, kEnd = 4 };
 
@@ -55,12 +54,15 @@ struct UnitSlot {
   float s[2 * kUnitPieces];
 };
 
+template <int NS, int NW>
 struct Smem {
-  alignas(128) unsigned char ring[kNS][kPieceBytes];
-  uint64_t full[kNS];
-  uint64_t empty[kNS];
-  StageMeta meta[kNS];
-  UnitSlot unit[kNS];
+  static constexpr int NU = 2 * NS;  // unit slots
+  alignas(128) unsigned char ring[NS][kPieceBytes];
+  uint64_t full[NS];
+  uint64_t empty[NS];
+  uint64_t ufree[NU];
+  StageMeta meta[NS];
+  UnitSlot unit[NU];
 };
 
 // ---------------------------------------------------------------------------
@@ -134,46 +136,57 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, const DenseParams& P)
   return true;
 }
 
-// producer lane 0: wait until row b's stop constants are published
-__device__ bool wait_ready(const DenseParams& P, int b) {
-  const uint32_t* rdy = ws_at<uint32_t>(P, P.L.ready) + b;
-  if (ld_acquire_u32(rdy)) return true;
-  WsHeader* h = hdr_of(P);
-  const long long t0 = clock64();
-  while (!ld_acquire_u32(rdy)) {
-    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return false;
-    if (clock64() - t0 > P.wait_bound) {
-      atomicOr(&h->status, kStatusTimeout);
-      atomicExch(&h->abort, 1u);
-      return false;
-    }
-    nanosleep_ns(128);
-  }
-  return true;
-}
-
 // ---------------------------------------------------------------------------
 // ticket -> work unit
 // ---------------------------------------------------------------------------
 struct Unit {
-  int resid, b, j, c;
+  int b, j, c;
 };
 
 __device__ __forceinline__ Unit decode_ticket(long long t, const DenseParams& P) {
-  long long rem;
-  int b, resid;
-  dense_ticket_row(t, P.B, P.G, P.g.nc_s, P.g.nc_r, P.lag, &resid, &b, &rem);
   Unit u;
-  u.resid = resid;
-  u.b = b;
-  if (!resid) {
-    u.j = (int)(rem / P.g.nc_s);
-    u.c = (int)(rem % P.g.nc_s);
-  } else {
-    u.j = 0;
-    u.c = (int)rem;
-  }
+  if (P.small_tickets)
+    dense_ticket_fast((unsigned)t, P.tk, &u.b, &u.j, &u.c);
+  else
+    dense_ticket(t, P.G, P.g.nc_s, &u.b, &u.j, &u.c);
   return u;
+}
+
+// residual queue entry: (row + 1) << 32 | unit, 0 while unpublished
+__device__ __forceinline__ unsigned long long* rq_of(const DenseParams& P) {
+  return ws_at<unsigned long long>(P, P.L.rq);
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// producer lane 0: wait until residual queue entry i is published (bounded)
+__device__ unsigned long long wait_entry(const DenseParams& P, unsigned i) {
+  const unsigned long long* e = rq_of(P) + i;
+  unsigned long long v = ld_acquire_u64(e);
+  if (v) return v;
+  WsHeader* h = hdr_of(P);
+  const long long t0 = clock64();
+  while (!(v = ld_acquire_u64(e))) {
+    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return 0;
+    if (clock64() - t0 > P.wait_bound) {
+      atomicOr(&h->status, kStatusTimeout);
+      atomicExch(&h->abort, 1u);
+      return 0;
+    }
+    nanosleep_ns(64);
+  }
+  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -193,7 +206,8 @@ __device__ __forceinline__ void copy_plain(unsigned char* dst, const unsigned ch
 }
 
 // fill stage `slot` with up to two row slices; completes full[slot]
-__device__ __forceinline__ void issue_stage(const DenseParams& P, Smem& S, int slot,
+template <int NS, int NW>
+__device__ __forceinline__ void issue_stage(const DenseParams& P, Smem<NS, NW>& S, int slot,
                                             const unsigned char* src0, int bytes0,
                                             const unsigned char* src1, int bytes1, int lane) {
   if (P.aligned) {
@@ -210,120 +224,238 @@ __device__ __forceinline__ void issue_stage(const DenseParams& P, Smem& S, int s
   }
 }
 
-__device__ void producer(const DenseParams& P, Smem& S, int lane) {
+template <int NS, int NW>
+__device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
+  constexpr int NU = Smem<NS, NW>::NU;
   WsHeader* h = hdr_of(P);
   const int G = P.G, V = P.V, es = P.g.es;
   uint32_t seq = 0, useq = 0;
   bool ok = true;
 
   auto acquire = [&](uint32_t s) -> bool {
-    if (s < (uint32_t)kNS) return true;
-    return wait_phase(&S.empty[s % kNS], ((s / kNS) - 1) & 1, P);
+    if (s < (uint32_t)NS) return true;
+    return wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P);
+  };
+  auto acquire_unit = [&](uint32_t u) -> bool {
+    if (u < (uint32_t)NU) return true;
+    return wait_phase(&S.ufree[u % NU], ((u / NU) - 1) & 1, P);
+  };
+  // Stage i of a unit is issued by lane i: its own ring-slot wait, metadata,
+  // expect-tx and bulk copy, so a whole unit costs one pass of the warp.
+  // (Rows that are not 16-byte aligned take the warp-wide plain-copy path.)
+  auto lane_acquire = [&](bool mine, uint32_t s) -> bool {
+    bool ok_l = true;
+    if (mine && s >= (uint32_t)NS) ok_l = wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P);
+    return __all_sync(0xffffffffu, ok_l);
   };
 
-  while (ok) {
-    unsigned long long t = 0;
-    if (lane == 0) t = atomicAdd(&h->ticket, 1ull);
-    t = __shfl_sync(0xffffffffu, t, 0);
-    if ((long long)t >= P.tickets) break;
-    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) break;
-    const Unit u = decode_ticket((long long)t, P);
-    if (!u.resid) {
-      const int npc = min(kUnitPieces, P.g.np_s - u.c * kUnitPieces);
-      const int up = (u.j < G) ? 2 * npc : npc;
-      const int uslot = useq % kNS;
-      ++useq;
-      for (int pi = 0; pi < up; ++pi) {
+  auto issue_stats = [&](const Unit& u) -> bool {
+    if (!acquire_unit(useq)) return false;
+    const int uslot = useq % NU;
+    ++useq;
+    const int npc = min(kUnitPieces, P.g.np_s - u.c * kUnitPieces);
+    const int up = (u.j < G) ? 2 * npc : npc;
+    if (P.aligned) {
+      const int pi = lane;
+      const bool mine = pi < up;
+      const uint32_t sq = seq + (uint32_t)pi;
+      if (!lane_acquire(mine, sq)) return false;
+      if (mine) {
         const int isd = pi >= npc;
         const int kp = u.c * kUnitPieces + (isd ? pi - npc : pi);
         const int ne = min(P.g.pe, V - kp * P.g.pe);
         const unsigned char* row = isd ? draft_row(P, u.b, u.j) : target_row(P, u.b, u.j);
-        if (!(ok = acquire(seq))) break;
-        const int slot = seq % kNS;
-        if (lane == 0) {
-          StageMeta& m = S.meta[slot];
-          m.kind = isd ? kStatsD : kStatsT;
-          m.b = u.b;
-          m.j = u.j;
-          m.kp = kp;
-          m.ne = ne;
-          m.uslot = uslot;
-          m.upieces = up;
-          m.pidx = pi;
-          m.unit_c = u.c;
-          m.npc = npc;
-        }
-        issue_stage(P, S, slot, row + (size_t)kp * kPieceBytes, ne * es, nullptr, 0, lane);
-        ++seq;
+        const int slot = sq % NS;
+        StageMeta& m = S.meta[slot];
+        m.kind = isd ? kStatsD : kStatsT;
+        m.b = u.b;
+        m.j = u.j;
+        m.kp = kp;
+        m.ne = ne;
+        m.uslot = uslot;
+        m.upieces = up;
+        m.pidx = pi;
+        m.unit_c = u.c;
+        m.npc = npc;
+        mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(ne * es));
+        bulk_g2s(S.ring[slot], row + (size_t)kp * kPieceBytes, (uint32_t)(ne * es), &S.full[slot]);
       }
-    } else {
-      uint32_t rdy = 1;
-      if (lane == 0) rdy = wait_ready(P, u.b) ? 1u : 0u;
-      rdy = __shfl_sync(0xffffffffu, rdy, 0);
+      seq += (uint32_t)up;
+      return true;
+    }
+    for (int pi = 0; pi < up; ++pi) {
+      const int isd = pi >= npc;
+      const int kp = u.c * kUnitPieces + (isd ? pi - npc : pi);
+      const int ne = min(P.g.pe, V - kp * P.g.pe);
+      const unsigned char* row = isd ? draft_row(P, u.b, u.j) : target_row(P, u.b, u.j);
+      if (!acquire(seq)) return false;
+      const int slot = seq % NS;
+      if (lane == 0) {
+        StageMeta& m = S.meta[slot];
+        m.kind = isd ? kStatsD : kStatsT;
+        m.b = u.b;
+        m.j = u.j;
+        m.kp = kp;
+        m.ne = ne;
+        m.uslot = uslot;
+        m.upieces = up;
+        m.pidx = pi;
+        m.unit_c = u.c;
+        m.npc = npc;
+      }
+      issue_stage(P, S, slot, row + (size_t)kp * kPieceBytes, ne * es, nullptr, 0, lane);
+      ++seq;
+    }
+    return true;
+  };
+
+  // residual unit (b, c) of a row whose stop constants are published
+  auto issue_resid = [&](int b, int c) -> bool {
+    if (!acquire_unit(useq)) return false;
+    const int uslot = useq % NU;
+    ++useq;
+    const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
+    const int npc = min(kUnitPieces, P.g.np_r - c * kUnitPieces);
+    const unsigned char* trow = target_row(P, b, st.n);
+    const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
+    auto fill_meta = [&](StageMeta& m, int kp, int ne, int pi) {
+      m.kind = (st.mode == 2) ? kResidSkip : kResid;
+      m.b = b;
+      m.j = st.n;
+      m.kp = kp;
+      m.ne = ne;
+      m.uslot = uslot;
+      m.upieces = npc;
+      m.pidx = pi;
+      m.unit_c = c;
+      m.npc = npc;
+      m.mode = st.mode;
+      m.ct = st.ct;
+      m.cd = st.cd;
+      m.invSt = st.invSt;
+      m.invSd = st.invSd;
+    };
+    if (P.aligned || st.mode == 2) {
+      const int pi = lane;
+      const bool mine = pi < npc;
+      const uint32_t sq = seq + (uint32_t)pi;
+      if (!lane_acquire(mine, sq)) return false;
+      if (mine) {
+        const int kp = c * kUnitPieces + pi;
+        const int ne = min(P.g.re, V - kp * P.g.re);
+        const int slot = sq % NS;
+        fill_meta(S.meta[slot], kp, ne, pi);
+        if (st.mode == 2) {
+          mbar_arrive(&S.full[slot]);
+        } else {
+          const size_t off = (size_t)kp * kResidRowBytes;
+          const uint32_t bytes = (uint32_t)(ne * es);
+          mbar_arrive_expect_tx(&S.full[slot], drow ? 2 * bytes : bytes);
+          bulk_g2s(S.ring[slot], trow + off, bytes, &S.full[slot]);
+          if (drow) bulk_g2s(S.ring[slot] + kResidRowBytes, drow + off, bytes, &S.full[slot]);
+        }
+      }
+      seq += (uint32_t)npc;
+      return true;
+    }
+    for (int pi = 0; pi < npc; ++pi) {
+      const int kp = c * kUnitPieces + pi;
+      const int ne = min(P.g.re, V - kp * P.g.re);
+      if (!acquire(seq)) return false;
+      const int slot = seq % NS;
+      if (lane == 0) fill_meta(S.meta[slot], kp, ne, pi);
+      const size_t off = (size_t)kp * kResidRowBytes;
+      issue_stage(P, S, slot, trow + off, ne * es, drow ? drow + off : nullptr,
+                  drow ? ne * es : 0, lane);
+      ++seq;
+    }
+    return true;
+  };
+
+  // Work loop.  Ready residual work (published by row finalisers) is taken
+  // first -- its rows were just read and are still in L2 -- otherwise the next
+  // statistics ticket.  A claimed but not yet published queue entry is only
+  // waited for when no statistics ticket is left, so no producer ever blocks
+  // while holding statistics work.
+  WsHeader* hq = h;
+  unsigned long long next = 0;  // prefetched statistics ticket
+  uint32_t v_head = 0, v_res = 0;  // last seen queue counters (loaded a unit ahead)
+  if (lane == 0) {
+    next = atomicAdd(&h->ticket, 1ull);
+    v_head = ld_relaxed_u32(&hq->rq_head);
+    v_res = ld_relaxed_u32(&hq->rq_reserve);
+  }
+  long long held = -1;  // claimed queue entry not yet issued
+  while (ok) {
+    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
+      ok = false;
+      break;
+    }
+    const unsigned long long t = __shfl_sync(0xffffffffu, next, 0);
+    const bool stats_left = (long long)t < P.tickets;
+    // try to claim residual work the counters say is published
+    if (held < 0) {
+      uint32_t claim = 0xffffffffu;
+      if (lane == 0) {
+        const bool avail = v_head < v_res;
+        if (avail || !stats_left) claim = atomicAdd(&hq->rq_head, 1u);
+        v_head = ld_relaxed_u32(&hq->rq_head);
+        v_res = ld_relaxed_u32(&hq->rq_reserve);
+      }
+      claim = __shfl_sync(0xffffffffu, claim, 0);
+      if (claim != 0xffffffffu) {
+        if (claim >= P.resid_units) {
+          if (!stats_left) break;  // every residual unit is claimed: done
+        } else {
+          held = claim;
+        }
+      }
+    }
+    if (held >= 0) {
+      unsigned long long e = 0;
+      if (lane == 0) {
+        e = ld_acquire_u64(rq_of(P) + held);
+        if (!e && !stats_left) e = wait_entry(P, (unsigned)held);
+      }
+      e = __shfl_sync(0xffffffffu, e, 0);
       __syncwarp();
-      if (!rdy) {
+      if (e) {
+        if (lane == 0) rq_of(P)[held] = 0ull;  // self-reset for the next call
+        held = -1;
+        ok = issue_resid((int)(e >> 32) - 1, (int)(e & 0xffffffffu));
+        continue;
+      }
+      if (!stats_left) {  // the bounded wait ran out
         ok = false;
         break;
       }
-      const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + u.b);
-      const int npc = min(kUnitPieces, P.g.np_r - u.c * kUnitPieces);
-      const int uslot = useq % kNS;
-      ++useq;
-      const unsigned char* trow = target_row(P, u.b, st.n);
-      const unsigned char* drow = (st.mode == 0) ? draft_row(P, u.b, st.n) : nullptr;
-      for (int pi = 0; pi < npc; ++pi) {
-        const int kp = u.c * kUnitPieces + pi;
-        const int ne = min(P.g.re, V - kp * P.g.re);
-        if (!(ok = acquire(seq))) break;
-        const int slot = seq % kNS;
-        if (lane == 0) {
-          StageMeta& m = S.meta[slot];
-          m.kind = (st.mode == 2) ? kResidSkip : kResid;
-          m.b = u.b;
-          m.j = st.n;
-          m.kp = kp;
-          m.ne = ne;
-          m.uslot = uslot;
-          m.upieces = npc;
-          m.pidx = pi;
-          m.unit_c = u.c;
-          m.npc = npc;
-          m.mode = st.mode;
-          m.ct = st.ct;
-          m.cd = st.cd;
-          m.invSt = st.invSt;
-          m.invSd = st.invSd;
-        }
-        if (st.mode == 2) {
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&S.full[slot]);
-        } else {
-          const size_t off = (size_t)kp * kResidRowBytes;
-          issue_stage(P, S, slot, trow + off, ne * es, drow ? drow + off : nullptr,
-                      drow ? ne * es : 0, lane);
-        }
-        ++seq;
-      }
+    }
+    if (stats_left) {
+      if (lane == 0) next = atomicAdd(&h->ticket, 1ull);  // prefetch the next ticket
+      ok = issue_stats(decode_ticket((long long)t, P));
     }
   }
-  // one end marker per consumer warp
-  for (int w = 0; w < kNW && ok; ++w) {
-    if (!(ok = acquire(seq))) break;
-    const int slot = seq % kNS;
-    if (lane == 0) {
+  // one end marker per consumer warp (lane w marks the stage consumer w takes next)
+  static_assert(NW <= 32, "one lane per consumer warp");
+  if (ok) {
+    const bool mine = lane < NW;
+    const uint32_t sq = seq + (uint32_t)lane;
+    ok = lane_acquire(mine, sq);
+    if (ok && mine) {
+      const int slot = sq % NS;
       S.meta[slot].kind = kEnd;
       mbar_arrive(&S.full[slot]);
     }
-    ++seq;
+    seq += NW;
   }
   // never leave the CTA with bulk copies in flight
   if (lane == 0) {
-    const uint32_t first = seq > (uint32_t)kNS ? seq - kNS : 0u;
+    const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0u;
     for (uint32_t s = first; s < seq; ++s) {
-      const int slot = s % kNS;
-      if (!mbar_try_wait(&S.full[slot], (s / kNS) & 1)) {
+      const int slot = s % NS;
+      if (!mbar_try_wait(&S.full[slot], (s / NS) & 1)) {
         const long long t0 = clock64();
-        while (!mbar_try_wait(&S.full[slot], (s / kNS) & 1) && clock64() - t0 < P.wait_bound) {
+        while (!mbar_try_wait(&S.full[slot], (s / NS) & 1) && clock64() - t0 < P.wait_bound) {
         }
       }
     }
@@ -331,10 +463,12 @@ __device__ void producer(const DenseParams& P, Smem& S, int lane) {
 }
 
 // ---------------------------------------------------------------------------
-// consumer: statistics of one 4 KB piece
+// consumer: statistics of one 4 KB piece.  Releases the stage (`release`)
+// as soon as every loaded register has been consumed.
 // ---------------------------------------------------------------------------
+template <class Release>
 __device__ __forceinline__ void stats_piece(const unsigned char* slot, int ne, int bf16, int lane,
-                                            float& c_out, float& s_out) {
+                                            float& c_out, float& s_out, Release release) {
   const uint4* v = reinterpret_cast<const uint4*>(slot);
   constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // two bf16 -inf
   uint4 r[8];
@@ -380,6 +514,8 @@ __device__ __forceinline__ void stats_piece(const unsigned char* slot, int ne, i
       m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(r[i].x), __uint_as_float(r[i].y)),
                          fmaxf(__uint_as_float(r[i].z), __uint_as_float(r[i].w))));
   }
+  // every loaded register has been read by the max: hand the stage back
+  release();
   m = warp_max(m);
   // c = log2e * max; an all -inf piece keeps c = 0 so NaN inputs still poison s
   const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
@@ -450,85 +586,63 @@ __device__ __forceinline__ float resid_piece(const unsigned char* slot, const St
 // ---------------------------------------------------------------------------
 // hand-offs: position -> row -> residual -> token
 // ---------------------------------------------------------------------------
-__device__ void final_select(const DenseParams& P, int b, int lane);
-
+// Last statistics unit of row b: combine every position's unit partials, run
+// all accept tests (lane j = position j, in fp64), find the first rejection n
+// and publish the stop constants.  One fence, one release.
 __device__ void finalize_row(const DenseParams& P, int b, int lane) {
   __threadfence();
-  const int G = P.G;
-  const PosInfo* pp = ws_at<PosInfo>(P, P.L.pos) + (size_t)b * (G + 1);
-  int n = G, err = 0;
+  const int G = P.G, nc = P.g.nc_s;
+  const UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
+  int n = G, err_any = 0, have_stop = 0;
+  float s_ct = 0.f, s_cd = 0.f;
+  double s_St = 1.0, s_Sd = 1.0;
   for (int j0 = 0; j0 <= G; j0 += 32) {
     const int j = j0 + lane;
-    int e = 0, rej = 0;
-    if (j <= G) {
-      const PosInfo q = ldcg32(pp + j);
-      e = q.err;
-      rej = (j < G) && !q.accept;
+    const bool on = j <= G;
+    int err = 0, x = 0;
+    float tx = 0.f, dx = 0.f;
+    if (on && j < G) {
+      x = P.x[(size_t)b * G + j];
+      if (x < 0 || x >= P.V) {
+        err = 1;
+      } else {
+        tx = load_logit(target_row(P, b, j), x, P.bf16);
+        dx = load_logit(draft_row(P, b, j), x, P.bf16);
+      }
     }
-    err |= __any_sync(0xffffffffu, e);
-    const unsigned bal = __ballot_sync(0xffffffffu, rej);
-    if (bal && n == G) n = j0 + __ffs(bal) - 1;
-  }
-  if (lane == 0) {
-    StopInfo st;
-    st.n = n;
-    st.T = 0.0;
-    if (err) {
-      st.mode = 2;
-      st.ct = st.cd = st.invSt = st.invSd = 0.f;
-    } else if (n < G) {
-      const PosInfo q = ldcg32(pp + n);
-      st.mode = 0;
-      st.ct = q.ct;
-      st.cd = q.cd;
-      st.invSt = (float)(1.0 / q.St);
-      st.invSd = (float)(1.0 / q.Sd);
-    } else {
-      const PosInfo q = ldcg32(pp + G);
-      st.mode = 1;
-      st.ct = q.ct;
-      st.cd = 0.f;
-      st.invSt = (float)(1.0 / q.St);
-      st.invSd = 0.f;
+    // online combination of the position's unit partials
+    float Ct = -INFINITY, Cd = -INFINITY;
+    double St = 0.0, Sd = 0.0;
+    if (on) {
+      const UnitPart* up = up_row + (size_t)j * nc;
+#pragma unroll 4
+      for (int k = 0; k < nc; ++k) {
+        const UnitPart u = ldcg32(up + k);
+        if (u.ct > Ct) {
+          St = St * (double)part_scale(Ct, u.ct) + u.St;
+          Ct = u.ct;
+        } else {
+          St += u.St * (double)part_scale(u.ct, Ct);
+        }
+        if (u.cd > Cd) {
+          Sd = Sd * (double)part_scale(Cd, u.cd) + u.Sd;
+          Cd = u.cd;
+        } else {
+          Sd += u.Sd * (double)part_scale(u.cd, Cd);
+        }
+      }
+      err |= !(Ct > -INFINITY && Ct < INFINITY && St > 0.0 && St < INFINITY);
+      if (j < G) err |= !(Cd > -INFINITY && Cd < INFINITY && Sd > 0.0 && Sd < INFINITY);
+      // consumed: leave the workspace zero for the next call
+      for (int k = 0; k < nc; ++k) {
+        int4* q = reinterpret_cast<int4*>(const_cast<UnitPart*>(up + k));
+        q[0] = make_int4(0, 0, 0, 0);
+        q[1] = make_int4(0, 0, 0, 0);
+      }
     }
-    ws_at<StopInfo>(P, P.L.stop)[b] = st;
-    ws_at<uint32_t>(P, P.L.cnt_row)[b] = 0;
-    __threadfence();
-    st_release_u32(ws_at<uint32_t>(P, P.L.ready) + b, 1u);
-  }
-  __syncwarp();
-}
-
-__device__ void finalize_position(const DenseParams& P, int b, int j, int lane) {
-  __threadfence();
-  const int G = P.G, nc = P.g.nc_s;
-  const UnitPart* up = ws_at<UnitPart>(P, P.L.upart) + ((size_t)b * (G + 1) + j) * nc;
-  float Ct = -INFINITY, Cd = -INFINITY;
-  for (int k = lane; k < nc; k += 32) {
-    const UnitPart u = ldcg32(up + k);
-    Ct = fmaxf(Ct, u.ct);
-    Cd = fmaxf(Cd, u.cd);
-  }
-  Ct = warp_max(Ct);
-  Cd = warp_max(Cd);
-  double St = 0.0, Sd = 0.0;
-  for (int k = lane; k < nc; k += 32) {
-    const UnitPart u = ldcg32(up + k);
-    St += u.St * (double)part_scale(u.ct, Ct);
-    Sd += u.Sd * (double)part_scale(u.cd, Cd);
-  }
-  St = warp_sum_d(St);
-  Sd = warp_sum_d(Sd);
-  int err = !(Ct > -INFINITY && Ct < INFINITY && St > 0.0 && St < INFINITY);
-  if (j < G) err |= !(Cd > -INFINITY && Cd < INFINITY && Sd > 0.0 && Sd < INFINITY);
-  int acc = 0;
-  double a = 0.0;
-  if (j < G) {
-    const int x = P.x[(size_t)b * G + j];
-    if (x < 0 || x >= P.V) err = 1;
-    if (!err) {
-      const float tx = load_logit(target_row(P, b, j), x, P.bf16);
-      const float dx = load_logit(draft_row(P, b, j), x, P.bf16);
+    int acc = 1;
+    double a = 0.0;
+    if (on && j < G && !err) {
       const double L = (double)kLog2e;
       const double p = (tx == -INFINITY) ? 0.0 : exp2((double)tx * L - (double)Ct) / St;
       const double q = (dx == -INFINITY) ? 0.0 : exp2((double)dx * L - (double)Cd) / Sd;
@@ -536,30 +650,117 @@ __device__ void finalize_position(const DenseParams& P, int b, int j, int lane) 
       a = ratio < 1.0 ? ratio : 1.0;
       acc = (double)P.u_acc[(size_t)b * G + j] < a;
     }
+    if (on && j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : (float)a;
+    err_any |= __any_sync(0xffffffffu, on && err);
+    const unsigned rej = __ballot_sync(0xffffffffu, on && j < G && !acc);
+    int src = -1;
+    if (!have_stop && rej) {
+      n = j0 + __ffs(rej) - 1;
+      src = n - j0;
+    } else if (!have_stop && G <= j0 + 31) {
+      src = G - j0;  // no rejection anywhere: the bonus position
+    }
+    if (src >= 0) {
+      have_stop = 1;
+      s_ct = __shfl_sync(0xffffffffu, Ct, src);
+      s_cd = __shfl_sync(0xffffffffu, Cd, src);
+      s_St = __shfl_sync(0xffffffffu, St, src);
+      s_Sd = __shfl_sync(0xffffffffu, Sd, src);
+    }
   }
-  int row_done = 0;
   if (lane == 0) {
-    PosInfo pi;
-    pi.St = St;
-    pi.Sd = Sd;
-    pi.ct = Ct;
-    pi.cd = Cd;
-    pi.accept = acc;
-    pi.err = err;
-    ws_at<PosInfo>(P, P.L.pos)[(size_t)b * (G + 1) + j] = pi;
-    if (P.acc_out && j < G) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : (float)a;
-    if (err) atomicOr(&hdr_of(P)->status, kStatusInputErr);
-    ws_at<uint32_t>(P, P.L.cnt_pos)[(size_t)b * (G + 1) + j] = 0;
+    StopInfo st;
+    st.n = n;
+    st.T = 0.0;
+    if (err_any) {
+      st.mode = 2;
+      st.ct = st.cd = st.invSt = st.invSd = 0.f;
+      atomicOr(&hdr_of(P)->status, kStatusInputErr);
+    } else if (n < G) {
+      st.mode = 0;
+      st.ct = s_ct;
+      st.cd = s_cd;
+      st.invSt = (float)(1.0 / s_St);
+      st.invSd = (float)(1.0 / s_Sd);
+    } else {
+      st.mode = 1;
+      st.ct = s_ct;
+      st.cd = 0.f;
+      st.invSt = (float)(1.0 / s_St);
+      st.invSd = 0.f;
+    }
+    ws_at<StopInfo>(P, P.L.stop)[b] = st;
+    ws_at<uint32_t>(P, P.L.cnt_row)[b] = 0;
     __threadfence();
-    const unsigned o = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + b, 1u);
-    row_done = (o == (unsigned)G);
   }
-  row_done = __shfl_sync(0xffffffffu, row_done, 0);
-  if (row_done) finalize_row(P, b, lane);
+  // publish the row's residual units to the queue
+  unsigned base = 0;
+  if (lane == 0) base = atomicAdd(&hdr_of(P)->rq_reserve, (unsigned)P.g.nc_r);
+  base = __shfl_sync(0xffffffffu, base, 0);
+  __syncwarp();
+  for (int c = lane; c < P.g.nc_r; c += 32)
+    st_release_u64(rq_of(P) + base + c, ((unsigned long long)(b + 1) << 32) | (unsigned)c);
+  __syncwarp();
+}
+
+// The residual (or p) values of one residual piece for the final walk: lane l
+// holds the piece's elements [l*per, (l+1)*per) in ascending order, loaded
+// with 16-byte vectors when the rows are aligned.  Values are bit-identical
+// to those resid_piece summed.
+template <int BF16>
+__device__ __forceinline__ void piece_values(const DenseParams& P, const unsigned char* trow,
+                                             const unsigned char* drow, int y0, int ne,
+                                             const StopInfo& st, int lane, float (&rv)[32]) {
+  constexpr int per = BF16 ? 32 : 16;  // elements per lane (64 bytes)
+  const int e0 = lane * per;
+  if (P.aligned && e0 + per <= ne) {
+    const uint4* tv = reinterpret_cast<const uint4*>(trow + (size_t)(y0 + e0) * (BF16 ? 2 : 4));
+    const uint4* dv = drow ? reinterpret_cast<const uint4*>(drow + (size_t)(y0 + e0) * (BF16 ? 2 : 4))
+                           : nullptr;
+    uint4 t4[4], d4[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      t4[i] = __ldcg(tv + i);
+      d4[i] = dv ? __ldcg(dv + i) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t* tw = reinterpret_cast<const uint32_t*>(&t4[i]);
+      const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d4[i]);
+      if (BF16) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float t = (e & 1) ? bf16_hi(tw[e >> 1]) : bf16_lo(tw[e >> 1]);
+          const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+          rv[i * 8 + e] = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          rv[i * 4 + e] = resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), st.ct, st.cd,
+                                    st.invSt, st.invSd, st.mode);
+      }
+    }
+#pragma unroll
+    for (int e = per; e < 32; ++e) rv[e] = 0.f;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      const int y = e0 + e;
+      float r = 0.f;
+      if (e < per && y < ne) {
+        const float t = load_logit(trow, y0 + y, BF16);
+        const float d = drow ? load_logit(drow, y0 + y, BF16) : 0.f;
+        r = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
+      }
+      rv[e] = r;
+    }
+  }
 }
 
 // Select the token of row b from its per-piece masses (fp64 prefix over
 // pieces, then over the fp32 element values of the chosen piece).
+template <int BF16>
 __device__ void final_select(const DenseParams& P, int b, int lane) {
   __threadfence();
   const int G = P.G, V = P.V, np = P.g.np_r, re = P.g.re;
@@ -567,43 +768,39 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
   int32_t* tok = P.tok_out + (size_t)b * (G + 1);
   float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * np;
   const int n = st.n;
+  const float us = P.u_s[b];
   int y = -1;
   double T = 0.0;
   if (st.mode != 2) {
     const unsigned char* trow = target_row(P, b, n);
     const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, n) : nullptr;
     const int per = (np + 31) / 32;
-    for (int attempt = 0; attempt < 2; ++attempt) {
-      const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
-      double ls = 0.0;
-      for (int k = k0; k < k1; ++k) ls += (double)__ldcg(rm + k);
-      const double ex = warp_exclusive_scan_d(ls, lane);
-      T = __shfl_sync(0xffffffffu, ex + ls, 31);
-      if (!(T > 0.0) && st.mode == 0 && attempt == 0) {
-        // zero residual after a rejection (only through rounding): draw from p_n
-        st.mode = 1;
-        drow = nullptr;
-        for (int k = 0; k < np; ++k) {
-          const int y0 = k * re, ne = min(re, V - y0);
-          float s = 0.f;
-          for (int e = lane; e < ne; e += 32)
-            s += resid_val(load_logit(trow, y0 + e, P.bf16), 0.f, st.ct, st.cd, st.invSt,
-                           st.invSd, 1);
-          s = warp_sum(s);
-          if (lane == 0) rm[k] = s;
-        }
-        __threadfence();
-        __syncwarp();
-        continue;
-      }
-      break;
-    }
-    const double target = (double)P.u_s[b] * T;
-    // piece level
     const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
     double ls = 0.0;
     for (int k = k0; k < k1; ++k) ls += (double)__ldcg(rm + k);
-    const double ex = warp_exclusive_scan_d(ls, lane);
+    double ex = warp_exclusive_scan_d(ls, lane);
+    T = __shfl_sync(0xffffffffu, ex + ls, 31);
+    if (!(T > 0.0) && st.mode == 0) {
+      // zero residual after a rejection (only through rounding): draw from p_n
+      st.mode = 1;
+      drow = nullptr;
+      for (int k = 0; k < np; ++k) {
+        const int y0 = k * re, ne = min(re, V - y0);
+        float s = 0.f;
+        for (int e = lane; e < ne; e += 32)
+          s += resid_val(load_logit(trow, y0 + e, BF16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
+        s = warp_sum(s);
+        if (lane == 0) rm[k] = s;
+      }
+      __threadfence();
+      __syncwarp();
+      ls = 0.0;
+      for (int k = k0; k < k1; ++k) ls += (double)__ldcg(rm + k);
+      ex = warp_exclusive_scan_d(ls, lane);
+      T = __shfl_sync(0xffffffffu, ex + ls, 31);
+    }
+    const double target = (double)us * T;
+    // piece level
     const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && (ex + ls > target));
     int kstar = -1;
     double base = 0.0;
@@ -636,38 +833,36 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
       kstar = last < 0 ? 0 : last;
     }
-    // element level within piece kstar
+    // the masses are consumed: leave the workspace zero for the next call
+    for (int k = k0; k < k1; ++k) rm[k] = 0.f;
+    // element level within piece kstar (values in registers)
     const int y0 = kstar * re, ne = min(re, V - y0);
-    const int q = (ne + 31) / 32;
-    const int e0 = min(ne, lane * q), e1 = min(ne, e0 + q);
+    constexpr int per_lane = BF16 ? 32 : 16;
+    float rv[32];
+    piece_values<BF16>(P, trow, drow, y0, ne, st, lane, rv);
     double es = 0.0;
     int lastpos = -1;
-    for (int e = e0; e < e1; ++e) {
-      const float t = load_logit(trow, y0 + e, P.bf16);
-      const float d = drow ? load_logit(drow, y0 + e, P.bf16) : 0.f;
-      const float r = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
-      es += (double)r;
-      if (r > 0.f) lastpos = e;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+      es += (double)rv[e];
+      if (rv[e] > 0.f) lastpos = lane * per_lane + e;
     }
     const double eex = warp_exclusive_scan_d(es, lane);
     const double tl = target - base;
-    const unsigned ehit = clamp ? 0u : __ballot_sync(0xffffffffu, (e1 > e0) && (eex + es > tl));
+    const unsigned ehit = clamp ? 0u : __ballot_sync(0xffffffffu, eex + es > tl);
     if (ehit) {
       const int fl = __ffs(ehit) - 1;
-      if (lane == fl) {
-        double acc = base + eex;
-        for (int e = e0; e < e1; ++e) {
-          const float t = load_logit(trow, y0 + e, P.bf16);
-          const float d = drow ? load_logit(drow, y0 + e, P.bf16) : 0.f;
-          acc += (double)resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
-          if (acc > target) {
-            y = y0 + e;
-            break;
-          }
-        }
-        if (y < 0) y = y0 + (lastpos >= 0 ? lastpos : e1 - 1);
+      int yy = -1;
+      double acc = base + eex;
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        acc += (double)rv[e];
+        if (yy < 0 && acc > target) yy = lane * per_lane + e;
       }
-      y = __shfl_sync(0xffffffffu, y, fl);
+      if (yy < 0) yy = lastpos;
+      y = __shfl_sync(0xffffffffu, yy, fl);
+      if (y < 0) y = 0;
+      y += y0;
     } else {
       int lp = lastpos;
       for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
@@ -681,13 +876,20 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
     if (nn >= 0) v = (j < nn) ? P.x[(size_t)b * G + j] : (j == nn ? y : -1);
     tok[j] = v;
   }
+  if (st.mode == 2)  // an error row never reached the piece-level search
+    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
   if (lane == 0) {
     P.n_out[b] = nn;
     StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
-    sp->mode = st.mode;
-    sp->T = T;
+    if (P.keep_stop) {  // read (and cleared) by the residual-output kernel
+      sp->mode = st.mode;
+      sp->T = T;
+    } else {
+      int4* q = reinterpret_cast<int4*>(sp);
+      q[0] = make_int4(0, 0, 0, 0);
+      q[1] = make_int4(0, 0, 0, 0);
+    }
     ws_at<uint32_t>(P, P.L.cnt_res)[b] = 0;
-    ws_at<uint32_t>(P, P.L.ready)[b] = 0;
   }
   __syncwarp();
 }
@@ -695,17 +897,22 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
 // ---------------------------------------------------------------------------
 // consumer loop
 // ---------------------------------------------------------------------------
-__device__ void consumer(const DenseParams& P, Smem& S, int cw, int lane) {
+template <int NS, int NW>
+__device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane) {
   const int G = P.G;
-  for (uint32_t s = cw;; s += kNW) {
-    const int slot = s % kNS;
-    if (!wait_phase(&S.full[slot], (s / kNS) & 1, P)) break;
+  for (uint32_t s = cw;; s += NW) {
+    const int slot = s % NS;
+    if (!wait_phase(&S.full[slot], (s / NS) & 1, P)) break;
     const StageMeta m = S.meta[slot];
     if (m.kind == kEnd) break;
     UnitSlot& U = S.unit[m.uslot];
+    auto release = [&]() {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.empty[slot]);
+    };
     if (m.kind == kStatsT || m.kind == kStatsD) {
       float c, sm;
-      stats_piece(S.ring[slot], m.ne, P.bf16, lane, c, sm);
+      stats_piece(S.ring[slot], m.ne, P.bf16, lane, c, sm, release);
       unsigned old = 0;
       if (lane == 0) {
         U.c[m.pidx] = c;
@@ -714,7 +921,7 @@ __device__ void consumer(const DenseParams& P, Smem& S, int cw, int lane) {
         old = atomicAdd(&U.count, 1u);
       }
       old = __shfl_sync(0xffffffffu, old, 0);
-      int pos_done = 0;
+      int row_done = 0;
       if (old == (unsigned)m.upieces - 1) {
         __threadfence_block();
         __syncwarp();
@@ -728,6 +935,8 @@ __device__ void consumer(const DenseParams& P, Smem& S, int cw, int lane) {
         const double wd = (have && isd) ? (double)sl * (double)part_scale(cl, Cd) : 0.0;
         const double St = warp_sum_d(wt), Sd = warp_sum_d(wd);
         if (lane == 0) {
+          U.count = 0;
+          mbar_arrive(&S.ufree[m.uslot]);
           UnitPart u;
           u.St = St;
           u.Sd = Sd;
@@ -735,19 +944,16 @@ __device__ void consumer(const DenseParams& P, Smem& S, int cw, int lane) {
           u.cd = Cd;
           u.pad[0] = u.pad[1] = 0.f;
           ws_at<UnitPart>(P, P.L.upart)[((size_t)m.b * (G + 1) + m.j) * P.g.nc_s + m.unit_c] = u;
-          U.count = 0;
           __threadfence();
-          const unsigned o2 =
-              atomicAdd(ws_at<uint32_t>(P, P.L.cnt_pos) + (size_t)m.b * (G + 1) + m.j, 1u);
-          pos_done = (o2 == (unsigned)P.g.nc_s - 1);
+          const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + m.b, 1u);
+          row_done = (o2 == (unsigned)((G + 1) * P.g.nc_s) - 1);
         }
-        pos_done = __shfl_sync(0xffffffffu, pos_done, 0);
+        row_done = __shfl_sync(0xffffffffu, row_done, 0);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
-      if (pos_done) finalize_position(P, m.b, m.j, lane);
+      if (row_done) finalize_row(P, m.b, lane);
     } else {
       const float mass = (m.kind == kResid) ? resid_piece(S.ring[slot], m, P.bf16, lane) : 0.f;
+      release();
       unsigned old = 0;
       if (lane == 0) {
         U.s[m.pidx] = mass;
@@ -761,26 +967,36 @@ __device__ void consumer(const DenseParams& P, Smem& S, int cw, int lane) {
         float* rm = ws_at<float>(P, P.L.rmass) + (size_t)m.b * P.g.np_r + m.unit_c * kUnitPieces;
         for (int k = 0; k < m.upieces; ++k) rm[k] = U.s[k];
         U.count = 0;
+        mbar_arrive(&S.ufree[m.uslot]);
         __threadfence();
         const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_res) + m.b, 1u);
         row_done = (o2 == (unsigned)P.g.nc_r - 1);
       }
       row_done = __shfl_sync(0xffffffffu, row_done, 0);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
-      if (row_done) final_select(P, m.b, lane);
+      if (row_done) {
+        if (P.bf16)
+          final_select<1>(P, m.b, lane);
+        else
+          final_select<0>(P, m.b, lane);
+      }
     }
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) dense_verify_kernel(const __grid_constant__ DenseParams P) {
+template <int NS, int NW, int CTAS>
+__global__ void __launch_bounds__(32 * (NW + 1), CTAS)
+    dense_verify_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw);
+  using SM = Smem<NS, NW>;
+  SM& S = *reinterpret_cast<SM*>(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kNS; ++i) {
+    for (int i = 0; i < NS; ++i) {
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], 1);
+    }
+    for (int i = 0; i < SM::NU; ++i) {
+      mbar_init(&S.ufree[i], 1);
       S.unit[i].count = 0;
     }
     fence_mbar_init();
@@ -798,60 +1014,86 @@ __global__ void __launch_bounds__(kThreads, 1) dense_verify_kernel(const __grid_
     const unsigned prev = atomicAdd(&h->exit_cnt, 1u);
     if (prev == gridDim.x - 1) {
       h->ticket = 0ull;
+      h->rq_head = 0u;
+      h->rq_reserve = 0u;
       h->exit_cnt = 0u;
       __threadfence();
     }
   }
 }
 
-// residual_out: the distribution the emitted token was drawn from
+// residual_out: the distribution the emitted token was drawn from.  One CTA
+// per row; it clears the row's stop record once every thread has read it.
 __global__ void dense_resid_out_kernel(const __grid_constant__ DenseParams P, float* out) {
   const int b = blockIdx.x;
-  const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
+  StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
+  const StopInfo st = ldcg32(sp);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int4* q = reinterpret_cast<int4*>(sp);
+    q[0] = make_int4(0, 0, 0, 0);
+    q[1] = make_int4(0, 0, 0, 0);
+  }
   float* o = out + (size_t)b * P.V;
-  const int stride = gridDim.y * blockDim.x;
-  const int first = blockIdx.y * blockDim.x + threadIdx.x;
   if (st.mode == 2 || !(st.T > 0.0)) {
-    for (int y = first; y < P.V; y += stride) o[y] = 0.f;
+    for (int y = threadIdx.x; y < P.V; y += blockDim.x) o[y] = 0.f;
     return;
   }
   const unsigned char* trow = target_row(P, b, st.n);
   const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
   const double invT = 1.0 / st.T;
-  for (int y = first; y < P.V; y += stride) {
+  for (int y = threadIdx.x; y < P.V; y += blockDim.x) {
     const float t = load_logit(trow, y, P.bf16);
     const float d = drow ? load_logit(drow, y, P.bf16) : 0.f;
     o[y] = (float)((double)resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode) * invT);
   }
 }
 
+// kernel configurations: ring stages, consumer warps, CTAs per SM
+struct DenseConfig {
+  void (*fn)(DenseParams);
+  size_t smem;
+  int threads;
+  int ctas_per_sm;
+};
+
+template <int NS, int NW, int CTAS>
+DenseConfig make_config() {
+  DenseConfig c;
+  c.fn = dense_verify_kernel<NS, NW, CTAS>;
+  c.smem = sizeof(Smem<NS, NW>);
+  c.threads = 32 * (NW + 1);
+  c.ctas_per_sm = CTAS;
+  return c;
+}
+
+const DenseConfig& active_config() {
+  static const DenseConfig cfg = make_config<32, 16, 1>();
+  return cfg;
+}
+
 }  // namespace
 
-size_t dense_smem_bytes() { return sizeof(Smem); }
-int dense_ctas_per_sm() { return 1; }
+size_t dense_smem_bytes() { return active_config().smem; }
+int dense_ctas_per_sm() { return active_config().ctas_per_sm; }
 
 cudaError_t launch_dense(const DenseParams& p, int grid, cudaStream_t s) {
-  static int configured_dev = -1;
+  static bool configured[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (configured_dev != dev) {
-    e = cudaFuncSetAttribute(dense_verify_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(Smem));
+  const DenseConfig& c = active_config();
+  if (dev < 0 || dev >= 64 || !configured[dev]) {
+    e = cudaFuncSetAttribute(c.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
     if (e != cudaSuccess) return e;
-    configured_dev = dev;
+    if (dev >= 0 && dev < 64) configured[dev] = true;
   }
-  dense_verify_kernel<<<grid, kThreads, sizeof(Smem), s>>>(p);
+  c.fn<<<grid, c.threads, c.smem, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dense_resid_out(const DenseParams& p, float* resid_out, cudaStream_t s) {
-  const int threads = 256;
-  int gy = (p.V + threads * 4 - 1) / (threads * 4);
-  if (gy < 1) gy = 1;
-  if (gy > 65535) gy = 65535;
-  dim3 grid(p.B, gy);
-  dense_resid_out_kernel<<<grid, threads, 0, s>>>(p, resid_out);
+  dense_resid_out_kernel<<<p.B, 512, 0, s>>>(p, resid_out);
   return cudaGetLastError();
 }
 

@@ -14,11 +14,13 @@ namespace sv {
 enum : uint32_t { kStatusInputErr = 1u, kStatusTimeout = 2u };
 
 struct WsHeader {
-  unsigned long long ticket;  // dense persistent kernel: next work ticket
-  uint32_t exit_cnt;          // CTAs that finished (last one resets ticket)
+  unsigned long long ticket;  // dense persistent kernel: next statistics ticket
+  uint32_t exit_cnt;          // CTAs that finished (the last one resets the counters)
   uint32_t status;            // kStatus* bits, sticky until spec_verify_check
   uint32_t abort;             // set when a bounded wait ran out
-  uint32_t pad[59];
+  uint32_t rq_head;           // residual queue: next entry to claim
+  uint32_t rq_reserve;        // residual queue: entries reserved by row finalisers
+  uint32_t pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -59,14 +61,6 @@ struct UnitPart {
   float pad[2];
 };
 
-// Per (row, position) result of the accept test.
-struct PosInfo {
-  double St, Sd;  // normalisers relative to ct, cd
-  float ct, cd;
-  int32_t accept;
-  int32_t err;
-};
-
 // Per row: what the residual / bonus draw uses.  mode 0: residual
 // max(p_n - q_n, 0); mode 1: draw from p (bonus, or the zero-residual
 // fallback); mode 2: input error.
@@ -79,7 +73,7 @@ struct StopInfo {
 };
 
 struct DenseLayout {  // byte offsets into the workspace
-  size_t cnt_pos, cnt_row, cnt_res, ready, upart, pos, stop, rmass, total;
+  size_t cnt_row, cnt_res, rq, upart, stop, rmass, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -87,18 +81,14 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline DenseLayout dense_layout(long long B, int G, const DenseGeom& g) {
   DenseLayout L;
   size_t o = sizeof(WsHeader);
-  L.cnt_pos = o;
-  o = align_up(o + sizeof(uint32_t) * (size_t)B * (size_t)(G + 1), 256);
   L.cnt_row = o;
   o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
   L.cnt_res = o;
   o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
-  L.ready = o;
-  o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
+  L.rq = o;  // one 64-bit entry per residual unit; 0 = not yet published
+  o = align_up(o + sizeof(unsigned long long) * (size_t)B * (size_t)g.nc_r, 256);
   L.upart = o;
   o = align_up(o + sizeof(UnitPart) * (size_t)B * (size_t)(G + 1) * (size_t)g.nc_s, 256);
-  L.pos = o;
-  o = align_up(o + sizeof(PosInfo) * (size_t)B * (size_t)(G + 1), 256);
   L.stop = o;
   o = align_up(o + sizeof(StopInfo) * (size_t)B, 256);
   L.rmass = o;
@@ -113,41 +103,62 @@ inline DenseLayout dense_layout(long long B, int G, const DenseGeom& g) {
 #define SV_HD inline
 #endif
 
-// Ticket order of the dense persistent kernel.  Round r holds the statistics
-// units of row r (if r < B) followed by the residual units of row r - lag (if
-// r >= lag); Us = (G+1) * nc_s statistics units and Ur = nc_r residual units
-// per row.  Returns whether ticket t is a residual unit, its row, and its
-// index within that row's units of that kind.
-SV_HD void dense_ticket_row(long long t, long long B, int G, int nc_s, int nc_r, int lag,
-                            int* resid, int* b, long long* rem) {
-  const long long Us = (long long)(G + 1) * nc_s, Ur = nc_r, lg = lag;
-  const long long LA = lg < B ? lg : B;
-  const long long tA = LA * Us;
-  const long long nB = B > lg ? B - lg : 0;
-  const long long tB = tA + nB * (Us + Ur);
-  if (t < tA) {
-    *resid = 0;
-    *b = (int)(t / Us);
-    *rem = t % Us;
-  } else if (t < tB) {
-    const long long t2 = t - tA;
-    const long long r = lg + t2 / (Us + Ur);
-    const long long q = t2 % (Us + Ur);
-    if (q < Us) {
-      *resid = 0;
-      *b = (int)r;
-      *rem = q;
-    } else {
-      *resid = 1;
-      *b = (int)(r - lg);
-      *rem = q - Us;
-    }
-  } else {
-    const long long t2 = t - tB;
-    *resid = 1;
-    *b = (int)((B - LA) + t2 / Ur);
-    *rem = t2 % Ur;
-  }
+// Division of n < 2^31 by a fixed d >= 1 with one 64-bit multiply and a
+// shift: q = (n * m) >> (32 + sh), m = ceil(2^(32+sh) / d), sh = ceil(log2 d)
+// (Granlund and Montgomery's round-up method; exact because n * (m - 2^(32+sh)/d)
+// < 2^31 <= 2^(32+sh)/d for d <= 2^sh).
+struct FastDiv {
+  unsigned long long m;
+  unsigned d;
+  int sh;
+};
+
+inline FastDiv make_fastdiv(unsigned d) {
+  FastDiv f;
+  f.d = d;
+  int sh = 0;
+  while ((1ull << sh) < d) ++sh;
+  f.sh = sh;
+  const unsigned long long num = 1ull << (32 + sh);
+  f.m = num / d + ((num % d) ? 1ull : 0ull);
+  return f;
+}
+
+SV_HD unsigned fdiv(unsigned n, const FastDiv& f) {
+  return (unsigned)(((unsigned long long)n * f.m) >> (32 + f.sh));
+}
+
+// Statistics tickets are numbered row by row: ticket t is row b = t / Us,
+// position j and unit c with t - b * Us = j * nc_s + c (Us = (G+1) * nc_s).
+// Residual units are not ticketed: a row's finaliser publishes them to the
+// residual queue.
+SV_HD void dense_ticket(long long t, int G, int nc_s, int* b, int* j, int* c) {
+  const long long Us = (long long)(G + 1) * nc_s;
+  const long long bb = t / Us, rem = t - bb * Us;
+  *b = (int)bb;
+  *j = (int)(rem / nc_s);
+  *c = (int)(rem - (long long)(*j) * nc_s);
+}
+
+struct TicketConsts {
+  FastDiv div_us, div_ncs;
+};
+
+inline TicketConsts make_ticket_consts(int G, int nc_s) {
+  TicketConsts k;
+  k.div_us = make_fastdiv((unsigned)((G + 1) * nc_s));
+  k.div_ncs = make_fastdiv((unsigned)nc_s);
+  return k;
+}
+
+// dense_ticket for t < 2^31 with the precomputed dividers
+SV_HD void dense_ticket_fast(unsigned t, const TicketConsts& k, int* b, int* j, int* c) {
+  const unsigned bb = fdiv(t, k.div_us);
+  const unsigned rem = t - bb * k.div_us.d;
+  const unsigned jj = fdiv(rem, k.div_ncs);
+  *b = (int)bb;
+  *j = (int)jj;
+  *c = (int)(rem - jj * k.div_ncs.d);
 }
 
 struct DenseParams {
@@ -162,12 +173,15 @@ struct DenseParams {
   unsigned char* ws;
   DenseLayout L;
   DenseGeom g;
-  long long tickets;  // total work units
+  long long tickets;  // statistics units: B * (G+1) * nc_s
+  int small_tickets;  // 1: every ticket fits in 31 bits (32-bit decode)
+  unsigned resid_units;  // B * nc_r
+  TicketConsts tk;
   long long wait_bound;
   int B, G, V;
-  int bf16;     // 1: bf16 logits, 0: fp32
-  int aligned;  // 1: rows 16-byte aligned -> bulk copies
-  int lag;      // residual units of row r are scheduled after statistics of row r + lag
+  int bf16;       // 1: bf16 logits, 0: fp32
+  int aligned;    // 1: rows 16-byte aligned -> bulk copies
+  int keep_stop;  // 1: residual_out requested; its kernel reads and clears stop[]
 };
 
 // ---------------------------------------------------------------------------

@@ -1,7 +1,7 @@
 """The C-ABI library on a machine without a GPU: it loads, exports every
 symbol the headers declare, rejects bad arguments on the host before touching
 CUDA, sizes its workspace sanely, and its dense work schedule is a bijection
-onto the expected units with residual work always after its row's statistics."""
+onto the statistics units."""
 import ctypes
 import os
 import re
@@ -77,31 +77,29 @@ def test_host_validation_without_gpu(lib):
     assert lib.spec_verify_check(P, 0, P) == rs.SV_ERR_INVALID_ARG
 
 
-@pytest.mark.parametrize("B,G,V,es,lag", [(64, 7, 128256, 2, 4), (1, 15, 151936, 2, 3),
-                                           (5, 0, 3000, 4, 2), (3, 2, 100000, 4, 9),
-                                           (17, 31, 8192, 2, 1)])
-def test_dense_schedule_is_a_bijection(lib, B, G, V, es, lag):
-    pe, re_ = 4096 // es, 2048 // es
+@pytest.mark.parametrize("B,G,V,es", [(64, 7, 128256, 2), (1, 15, 151936, 2), (5, 0, 3000, 4),
+                                      (3, 2, 100000, 4), (17, 31, 8192, 2), (2, 255, 70001, 4)])
+def test_dense_statistics_schedule(lib, B, G, V, es):
+    """Tickets enumerate every (row, position, unit) once, in row order, and the
+    kernel's 32-bit decode agrees with plain division (rc 0)."""
+    pe = 4096 // es
     nc_s = -(-(-(-V // pe)) // 8)
-    nc_r = -(-(-(-V // re_)) // 8)
-    Us, Ur = (G + 1) * nc_s, nc_r
-    total = B * (Us + Ur)
-    seen = set()
-    last_stats = {}
-    first_resid = {}
+    total = B * (G + 1) * nc_s
+    seen = []
     for t in range(total):
-        resid, b, rem = rs.debug_dense_ticket(t, B, G, V, es, lag)
-        assert 0 <= b < B and 0 <= rem < (Ur if resid else Us)
-        key = (resid, b, rem)
-        assert key not in seen
-        seen.add(key)
-        if resid:
-            first_resid.setdefault(b, t)
-        else:
-            last_stats[b] = t
-    assert len(seen) == total
-    for b in range(B):
-        assert first_resid[b] > last_stats[b]  # a row's draw comes after all of its statistics
-        # ... and after the statistics of `lag` further rows when there are that many
-        if b + lag < B:
-            assert first_resid[b] > last_stats[b + lag]
+        seen.append(rs.debug_dense_ticket(t, B, G, V, es))
+    assert seen == [(b, j, c) for b in range(B) for j in range(G + 1) for c in range(nc_s)]
+    with pytest.raises(rs.SpecVerifyError):
+        rs.debug_dense_ticket(total, B, G, V, es)
+
+
+def test_fast_division_on_large_tickets(lib):
+    import numpy as np
+    rng = np.random.default_rng(0)
+    for (B, G, V, es) in [(1_000_000, 4, 50000, 2), (300_000, 63, 4097, 4), (7, 200, 2**24, 4)]:
+        pe = 4096 // es
+        nc_s = -(-(-(-V // pe)) // 8)
+        total = B * (G + 1) * nc_s
+        for t in list(rng.integers(0, min(total, 2**31 - 1), 2000)) + [0, min(total, 2**31) - 1]:
+            b, j, c = rs.debug_dense_ticket(int(t), B, G, V, es)
+            assert (b * (G + 1) + j) * nc_s + c == t

@@ -275,3 +275,29 @@ def test_repeated_calls_reuse_workspace_and_graph_replay():
         assert torch.equal(cap.n_accepted, first.n_accepted)
         assert torch.equal(cap.out_tokens, first.out_tokens)
     assert torch.equal(warm.out_tokens, first.out_tokens)
+
+
+def test_workspace_returns_to_zero_across_geometries():
+    """Every successful call leaves the whole workspace zero (apart from the
+    sticky status word), so calls of different sizes can share it."""
+    from rejection_sampling_gb300 import _binding as bnd
+    dev = torch.device("cuda", torch.cuda.current_device())
+    s = torch.cuda.Stream()
+    cases = [(3, 7, 20000, "bf16", True, False), (9, 1, 4096, "bf16", False, False),
+             (5, 3, 30000, "f32", True, True), (2, 40, 3000, "bf16", False, False),
+             (1, 15, 70001, "bf16", True, False), (12, 3, 9000, "f32", False, True)]
+    for (B, G, V, dt, resid, bad) in cases:
+        d = wl.dense_inputs(B, G, V, dtype=dt, seed=B + V)
+        if bad:
+            d["draft_ids"][0, 0] = V  # one invalid row
+        with torch.cuda.stream(s):
+            rs.spec_verify_dense(to_dev(d["target"]), to_dev(d["draft"]), to_dev(d["draft_ids"]),
+                                 to_dev(d["u_accept"]), to_dev(d["u_sample"]), residual=resid,
+                                 stream=s)
+        s.synchronize()
+        ws = bnd._ws_cache[(dev.index, s.cuda_stream)].cpu().numpy()
+        status = ws[12:16].view(np.uint32)[0]
+        ws[12:16] = 0
+        assert not ws.any(), (B, G, V, np.nonzero(ws)[0][:10])
+        assert status == (1 if bad else 0)
+        assert rs.check(dev, s) == (rs.SV_ERR_DEVICE_INPUT if bad else rs.SV_OK)
