@@ -16,8 +16,8 @@
 //    publishes the row's residual units -- up to 8 pieces of 2 KB target +
 //    2 KB draft of the stop position (b, n) -- to a queue that producers
 //    drain before taking new tickets.
-//  * Each CTA = 1 producer warp + NW consumer warps around an NS-stage ring of
-//    4 KB shared-memory stages.  The producer moves pieces with 1-D bulk
+//  * Each CTA = 1 producer warp + NW consumer warps + 1 finaliser warp around
+//    an NS-stage ring of 4 KB shared-memory stages.  The producer moves pieces with 1-D bulk
 //    copies (cp.async.bulk, TMA) completing on per-stage mbarriers; consumer
 //    warp w takes stages w, w + NW, ...  A consumer releases its stage as soon
 //    as the data is in registers, so slow bookkeeping never holds the ring.
@@ -26,7 +26,10 @@
 //    unit's pieces and publishes one partial; the last unit of a row runs all
 //    of the row's accept tests (one lane per position, fp64), finds the first
 //    rejection n and publishes the stop constants.  These
-//    hand-offs are last-arriver atomics: no warp ever waits for another CTA
+//    hand-offs are last-arriver atomics; the consumer that completes a row
+//    queues the row for its CTA's finaliser warp, so the latency of the
+//    row-level work never stalls the data pipeline.  No warp ever waits for
+//    another CTA
 //    while it holds statistics work.  A producer waits (bounded) for a queue
 //    entry only once every statistics ticket is taken; every such entry is
 //    published by a row whose statistics units are all held by running CTAs
@@ -54,8 +57,15 @@ struct UnitSlot {
   float s[2 * kUnitPieces];
 };
 
+constexpr int kFinQ = 64;  // finaliser queue entries
+
 template <int NS, int NW>
 struct Smem {
+  // Stage s lives in slot s % NS and is consumed by warp s % NW.  With NS a
+  // multiple of NW the stage that last used a slot (s - NS) belongs to the
+  // same warp, which consumed it first; a warp can therefore never wait on a
+  // slot two phases ahead, where an mbarrier parity wait would alias.
+  static_assert(NS % NW == 0, "ring depth must be a multiple of the consumer warps");
   static constexpr int NU = 2 * NS;  // unit slots
   alignas(128) unsigned char ring[NS][kPieceBytes];
   uint64_t full[NS];
@@ -63,6 +73,12 @@ struct Smem {
   uint64_t ufree[NU];
   StageMeta meta[NS];
   UnitSlot unit[NU];
+  // consumer -> finaliser hand-off: +(b+1) finalise row b, -(b+1) select its token
+  int fin_item[kFinQ];
+  unsigned fin_seq[kFinQ];
+  unsigned fin_tail;
+  unsigned fin_head;
+  unsigned cons_done;
 };
 
 // ---------------------------------------------------------------------------
@@ -116,9 +132,23 @@ __device__ __forceinline__ float resid_val(float t, float d, float ct, float cd,
 }
 
 // ---------------------------------------------------------------------------
-// bounded waits (every spin has a limit; on expiry: timeout + abort flags)
+// bounded waits (every spin has a limit; on expiry: timeout + abort flags and
+// the first expired site recorded in the header for diagnosis)
 // ---------------------------------------------------------------------------
-__device__ bool wait_phase(uint64_t* bar, uint32_t parity, const DenseParams& P) {
+enum WaitSite : unsigned {
+  kSiteProdEmpty = 1, kSiteProdUnit = 2, kSiteEntry = 4, kSiteConsFull = 5, kSiteFinPush = 6,
+  kSiteFinIdle = 7
+};
+
+__device__ void record_timeout(const DenseParams& P, unsigned site, unsigned info) {
+  WsHeader* h = hdr_of(P);
+  if (atomicCAS(&h->timeout_site, 0u, site) == 0u) h->timeout_info = info;
+  atomicOr(&h->status, kStatusTimeout);
+  atomicExch(&h->abort, 1u);
+}
+
+__device__ bool wait_phase(uint64_t* bar, uint32_t parity, const DenseParams& P, unsigned site,
+                           unsigned info) {
   if (mbar_try_wait(bar, parity)) return true;
   WsHeader* h = hdr_of(P);
   const long long t0 = clock64();
@@ -127,8 +157,7 @@ __device__ bool wait_phase(uint64_t* bar, uint32_t parity, const DenseParams& P)
     if ((++it & 63u) == 0) {
       if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return false;
       if (clock64() - t0 > P.wait_bound) {
-        atomicOr(&h->status, kStatusTimeout);
-        atomicExch(&h->abort, 1u);
+        record_timeout(P, site, info);
         return false;
       }
     }
@@ -180,8 +209,7 @@ __device__ unsigned long long wait_entry(const DenseParams& P, unsigned i) {
   while (!(v = ld_acquire_u64(e))) {
     if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return 0;
     if (clock64() - t0 > P.wait_bound) {
-      atomicOr(&h->status, kStatusTimeout);
-      atomicExch(&h->abort, 1u);
+      record_timeout(P, kSiteEntry, i);
       return 0;
     }
     nanosleep_ns(64);
@@ -234,18 +262,19 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
 
   auto acquire = [&](uint32_t s) -> bool {
     if (s < (uint32_t)NS) return true;
-    return wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P);
+    return wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P, kSiteProdEmpty, s);
   };
   auto acquire_unit = [&](uint32_t u) -> bool {
     if (u < (uint32_t)NU) return true;
-    return wait_phase(&S.ufree[u % NU], ((u / NU) - 1) & 1, P);
+    return wait_phase(&S.ufree[u % NU], ((u / NU) - 1) & 1, P, kSiteProdUnit, u);
   };
   // Stage i of a unit is issued by lane i: its own ring-slot wait, metadata,
   // expect-tx and bulk copy, so a whole unit costs one pass of the warp.
   // (Rows that are not 16-byte aligned take the warp-wide plain-copy path.)
   auto lane_acquire = [&](bool mine, uint32_t s) -> bool {
     bool ok_l = true;
-    if (mine && s >= (uint32_t)NS) ok_l = wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P);
+    if (mine && s >= (uint32_t)NS)
+      ok_l = wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P, kSiteProdEmpty, s);
     return __all_sync(0xffffffffu, ok_l);
   };
 
@@ -615,9 +644,20 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane) {
     double St = 0.0, Sd = 0.0;
     if (on) {
       const UnitPart* up = up_row + (size_t)j * nc;
-#pragma unroll 4
-      for (int k = 0; k < nc; ++k) {
-        const UnitPart u = ldcg32(up + k);
+      for (int k0 = 0; k0 < nc; k0 += 4) {
+        UnitPart buf[4];
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          if (k0 + kk < nc) {
+            buf[kk] = ldcg32(up + k0 + kk);
+          } else {
+            buf[kk].St = buf[kk].Sd = 0.0;
+            buf[kk].ct = buf[kk].cd = -INFINITY;
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+        const UnitPart& u = buf[kk];
         if (u.ct > Ct) {
           St = St * (double)part_scale(Ct, u.ct) + u.St;
           Ct = u.ct;
@@ -629,6 +669,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane) {
           Cd = u.cd;
         } else {
           Sd += u.Sd * (double)part_scale(u.cd, Cd);
+        }
         }
       }
       err |= !(Ct > -INFINITY && Ct < INFINITY && St > 0.0 && St < INFINITY);
@@ -897,12 +938,32 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
 // ---------------------------------------------------------------------------
 // consumer loop
 // ---------------------------------------------------------------------------
+// queue a row hand-off for this CTA's finaliser warp (lane 0 of a consumer)
+template <int NS, int NW>
+__device__ __forceinline__ void fin_push(const DenseParams& P, Smem<NS, NW>& S, int item, int lane) {
+  if (lane == 0) {
+    const unsigned pos = atomicAdd(&S.fin_tail, 1u);
+    // the queue has kFinQ entries; wait (bounded) while it is full
+    const long long t0 = clock64();
+    while (pos - *reinterpret_cast<volatile unsigned*>(&S.fin_head) >= (unsigned)kFinQ) {
+      if (clock64() - t0 > P.wait_bound) {
+        record_timeout(P, kSiteFinPush, pos);
+        break;
+      }
+      nanosleep_ns(32);
+    }
+    S.fin_item[pos % kFinQ] = item;
+    __threadfence_block();
+    *reinterpret_cast<volatile unsigned*>(&S.fin_seq[pos % kFinQ]) = pos + 1;
+  }
+  __syncwarp();
+}
 template <int NS, int NW>
 __device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane) {
   const int G = P.G;
   for (uint32_t s = cw;; s += NW) {
     const int slot = s % NS;
-    if (!wait_phase(&S.full[slot], (s / NS) & 1, P)) break;
+    if (!wait_phase(&S.full[slot], (s / NS) & 1, P, kSiteConsFull, s)) break;
     const StageMeta m = S.meta[slot];
     if (m.kind == kEnd) break;
     UnitSlot& U = S.unit[m.uslot];
@@ -950,7 +1011,7 @@ __device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane
         }
         row_done = __shfl_sync(0xffffffffu, row_done, 0);
       }
-      if (row_done) finalize_row(P, m.b, lane);
+      if (row_done) fin_push(P, S, m.b + 1, lane);
     } else {
       const float mass = (m.kind == kResid) ? resid_piece(S.ring[slot], m, P.bf16, lane) : 0.f;
       release();
@@ -973,18 +1034,73 @@ __device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane
         row_done = (o2 == (unsigned)P.g.nc_r - 1);
       }
       row_done = __shfl_sync(0xffffffffu, row_done, 0);
-      if (row_done) {
-        if (P.bf16)
-          final_select<1>(P, m.b, lane);
-        else
-          final_select<0>(P, m.b, lane);
-      }
+      if (row_done) fin_push(P, S, -(m.b + 1), lane);
     }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    atomicAdd(&S.cons_done, 1u);
   }
 }
 
+// finaliser warp: runs the row hand-offs the consumers queue, in order
+template <int NS, int NW>
+__device__ void finaliser(const DenseParams& P, Smem<NS, NW>& S, int lane) {
+  WsHeader* h = hdr_of(P);
+  unsigned head = 0;
+  long long t0 = clock64();
+  for (;;) {
+    int item = 0, state = 0;  // state 1: item, 2: done, 3: timeout/abort
+    if (lane == 0) {
+      const volatile unsigned* seq = S.fin_seq;
+      if (seq[head % kFinQ] == head + 1) {
+        __threadfence_block();
+        item = S.fin_item[head % kFinQ];
+        state = 1;
+      } else if (*reinterpret_cast<volatile unsigned*>(&S.cons_done) == (unsigned)NW &&
+                 *reinterpret_cast<volatile unsigned*>(&S.fin_tail) == head) {
+        state = 2;
+      } else if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
+        state = 3;
+      } else if (clock64() - t0 > 4 * P.wait_bound) {
+        // the finaliser only waits on its own CTA, whose waits have the
+        // shorter bound: a longer one here lets the root cause report first
+        record_timeout(P, kSiteFinIdle, head);
+        state = 3;
+      } else {
+        nanosleep_ns(32);
+      }
+    }
+    state = __shfl_sync(0xffffffffu, state, 0);
+    if (state >= 2) break;
+    if (state == 0) continue;
+    item = __shfl_sync(0xffffffffu, item, 0);
+    __syncwarp();
+    if (item > 0) {
+      finalize_row(P, item - 1, lane);
+    } else if (P.bf16) {
+      final_select<1>(P, -item - 1, lane);
+    } else {
+      final_select<0>(P, -item - 1, lane);
+    }
+    ++head;
+    if (lane == 0) *reinterpret_cast<volatile unsigned*>(&S.fin_head) = head;
+    t0 = clock64();
+  }
+}
+
+// register budget: each of the SM's four sub-partitions has 16K registers and
+// holds ceil(warps / 4) of the resident warps
+template <int NW, int CTAS>
+constexpr int dense_regs() {
+  constexpr int per_part = ((NW + 2) * CTAS + 3) / 4;
+  constexpr int r = 16384 / (32 * per_part) / 8 * 8;
+  return r > 255 ? 255 : r;
+}
+
 template <int NS, int NW, int CTAS>
-__global__ void __launch_bounds__(32 * (NW + 1), CTAS)
+__global__ void __maxnreg__((dense_regs<NW, CTAS>()))
     dense_verify_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   using SM = Smem<NS, NW>;
@@ -999,20 +1115,25 @@ __global__ void __launch_bounds__(32 * (NW + 1), CTAS)
       mbar_init(&S.ufree[i], 1);
       S.unit[i].count = 0;
     }
+    for (int i = 0; i < kFinQ; ++i) S.fin_seq[i] = 0u;
+    S.fin_tail = S.fin_head = S.cons_done = 0u;
     fence_mbar_init();
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
   if (warp == 0)
     producer(P, S, lane);
-  else
+  else if (warp <= NW)
     consumer(P, S, warp - 1, lane);
+  else
+    finaliser(P, S, lane);
   __syncthreads();
   if (threadIdx.x == 0) {
     WsHeader* h = hdr_of(P);
     __threadfence();
     const unsigned prev = atomicAdd(&h->exit_cnt, 1u);
-    if (prev == gridDim.x - 1) {
+    // after a timeout the counters are left as they are, for diagnosis
+    if (prev == gridDim.x - 1 && !*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
       h->ticket = 0ull;
       h->rq_head = 0u;
       h->rq_reserve = 0u;
@@ -1062,13 +1183,15 @@ DenseConfig make_config() {
   DenseConfig c;
   c.fn = dense_verify_kernel<NS, NW, CTAS>;
   c.smem = sizeof(Smem<NS, NW>);
-  c.threads = 32 * (NW + 1);
+  c.threads = 32 * (NW + 2);
   c.ctas_per_sm = CTAS;
   return c;
 }
 
 const DenseConfig& active_config() {
-  static const DenseConfig cfg = make_config<32, 16, 1>();
+  // 2 CTAs per SM, 24-stage rings, 8 consumer warps each (measured fastest of
+  // the configurations whose ring depth is a multiple of the consumer warps)
+  static const DenseConfig cfg = make_config<24, 8, 2>();
   return cfg;
 }
 

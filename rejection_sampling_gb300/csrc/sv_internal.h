@@ -20,7 +20,9 @@ struct WsHeader {
   uint32_t abort;             // set when a bounded wait ran out
   uint32_t rq_head;           // residual queue: next entry to claim
   uint32_t rq_reserve;        // residual queue: entries reserved by row finalisers
-  uint32_t pad[57];
+  uint32_t timeout_site;      // first wait that ran out (diagnostics; 0 = none)
+  uint32_t timeout_info;      // site-specific detail (slot, entry, ...)
+  uint32_t pad[55];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
