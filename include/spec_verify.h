@@ -112,7 +112,8 @@ sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream
  *   accept_prob_out [B, gamma] fp32 or NULL: min(1, p_j(x_j)/q_j(x_j)) for
  *                 every j (all positions are scored, as in the parallel pass)
  * Softmax, gather, ratio test, first-reject scan and the inverse-CDF draw run
- * in fp32 with fp64 combination of partial sums; bf16 inputs are widened
+ * in fp32, with partial sums combined and prefixed in float-float (pairs of
+ * fp32 carrying ~48 significant bits); bf16 inputs are widened
  * exactly.  One fused persistent kernel reads each logit once from HBM.
  */
 int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dtype dtype,

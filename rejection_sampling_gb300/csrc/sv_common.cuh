@@ -146,8 +146,108 @@ __device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// acquire-release fence at GPU scope: orders this thread's earlier memory
+// operations before its later ones for every observer on the GPU (lighter than
+// the sequentially consistent fence of __threadfence)
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) {
   asm volatile("nanosleep.u32 %0;" ::"r"(ns));
+}
+
+}  // namespace sv
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// float-float arithmetic (a value is hi + lo with |lo| <= ulp(hi)/2).
+// GB300's fp64 pipe is a small fraction of its fp32 rate, so sums that need
+// more than fp32 precision are carried as unevaluated pairs of floats, using
+// the error-free transformations two-sum (Knuth) and two-product (FMA).
+// Explicit _rn intrinsics keep the compiler from contracting or reordering.
+// ---------------------------------------------------------------------------
+struct ff {
+  float hi, lo;
+};
+
+__device__ __forceinline__ ff ff_make(float a) { return ff{a, 0.f}; }
+
+// s + e == a + b exactly
+__device__ __forceinline__ ff two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bv = __fsub_rn(s, a);
+  const float av = __fsub_rn(s, bv);
+  const float e = __fadd_rn(__fsub_rn(a, av), __fsub_rn(b, bv));
+  return ff{s, e};
+}
+
+// renormalise (|b| <= |a| or a == 0)
+__device__ __forceinline__ ff quick_two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  return ff{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+  ff s = two_sum(a.hi, b.hi);
+  const float e = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
+  return quick_two_sum(s.hi, e);
+}
+
+__device__ __forceinline__ ff ff_add_f(ff a, float b) {
+  ff s = two_sum(a.hi, b);
+  return quick_two_sum(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+__device__ __forceinline__ ff ff_neg(ff a) { return ff{-a.hi, -a.lo}; }
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff_neg(b)); }
+
+// a * b for floats, exactly as a pair
+__device__ __forceinline__ ff two_prod(float a, float b) {
+  const float p = __fmul_rn(a, b);
+  return ff{p, __fmaf_rn(a, b, -p)};
+}
+
+// ff * float
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+  ff p = two_prod(a.hi, b);
+  return quick_two_sum(p.hi, __fmaf_rn(a.lo, b, p.lo));
+}
+
+__device__ __forceinline__ float ff_to_f(ff a) { return __fadd_rn(a.hi, a.lo); }
+
+// sign of a - b
+__device__ __forceinline__ bool ff_gt(ff a, ff b) {
+  const ff d = ff_sub(a, b);
+  return d.hi > 0.f || (d.hi == 0.f && d.lo > 0.f);
+}
+
+__device__ __forceinline__ ff ff_shfl(ff a, int src) {
+  return ff{__shfl_sync(0xffffffffu, a.hi, src), __shfl_sync(0xffffffffu, a.lo, src)};
+}
+__device__ __forceinline__ ff ff_shfl_up(ff a, int d) {
+  return ff{__shfl_up_sync(0xffffffffu, a.hi, d), __shfl_up_sync(0xffffffffu, a.lo, d)};
+}
+__device__ __forceinline__ ff ff_shfl_xor(ff a, int m) {
+  return ff{__shfl_xor_sync(0xffffffffu, a.hi, m), __shfl_xor_sync(0xffffffffu, a.lo, m)};
+}
+
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = ff_add(v, ff_shfl_xor(v, o));
+  return v;
+}
+
+// exclusive prefix over lanes
+__device__ __forceinline__ ff warp_exclusive_scan_ff(ff v, int lane) {
+  ff x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff y = ff_shfl_up(x, o);
+    if (lane >= o) x = ff_add(x, y);
+  }
+  return ff_sub(x, v);
 }
 
 }  // namespace sv

@@ -24,7 +24,7 @@
 //  * A consumer warp reduces a 4 KB piece to (c, s): c = log2e * max, s =
 //    sum 2^(v*log2e - c) (MUFU ex2).  The last warp of a unit combines the
 //    unit's pieces and publishes one partial; the last unit of a row runs all
-//    of the row's accept tests (one lane per position, fp64), finds the first
+//    of the row's accept tests (one lane per position), finds the first
 //    rejection n and publishes the stop constants.  These
 //    hand-offs are last-arriver atomics; the consumer that completes a row
 //    queues the row for its CTA's finaliser warp, so the latency of the
@@ -37,7 +37,7 @@
 //  * Residual units recompute r(y) = max(p(y) - q(y), 0) for the stop
 //    position only (the rows are still in L2: they were read a few rows of
 //    work earlier) and publish per-piece masses; the last one selects the
-//    piece and then the token by an fp64 prefix over fp32 element values.
+//    piece and then the token by a float-float prefix over fp32 element values.
 #include "sv_common.cuh"
 
 namespace sv {
@@ -74,6 +74,7 @@ struct Smem {
   StageMeta meta[NS];
   UnitSlot unit[NU];
   // consumer -> finaliser hand-off: +(b+1) finalise row b, -(b+1) select its token
+  UnitPart fin_scratch[128];  // finaliser staging (4 KB)
   int fin_item[kFinQ];
   unsigned fin_seq[kFinQ];
   unsigned fin_tail;
@@ -193,6 +194,11 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -269,13 +275,39 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
     return wait_phase(&S.ufree[u % NU], ((u / NU) - 1) & 1, P, kSiteProdUnit, u);
   };
   // Stage i of a unit is issued by lane i: its own ring-slot wait, metadata,
-  // expect-tx and bulk copy, so a whole unit costs one pass of the warp.
-  // (Rows that are not 16-byte aligned take the warp-wide plain-copy path.)
+  // expect-tx and bulk copy.  A lane issues as soon as its slot is free, so the
+  // ring refills stage by stage rather than a whole unit at a time.  (Rows
+  // that are not 16-byte aligned take the warp-wide plain-copy path.)
   auto lane_acquire = [&](bool mine, uint32_t s) -> bool {
     bool ok_l = true;
     if (mine && s >= (uint32_t)NS)
       ok_l = wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P, kSiteProdEmpty, s);
     return __all_sync(0xffffffffu, ok_l);
+  };
+  // run issue(lane) on every lane with `mine` as soon as its stage's slot is free
+  auto lane_issue = [&](bool mine, uint32_t s, auto&& issue) -> bool {
+    bool pending = mine;
+    if (pending && s < (uint32_t)NS) {
+      issue();
+      pending = false;
+    }
+    const long long t0 = clock64();
+    unsigned it = 0;
+    while (__any_sync(0xffffffffu, pending)) {
+      if (pending && mbar_try_wait(&S.empty[s % NS], ((s / NS) - 1) & 1)) {
+        issue();
+        pending = false;
+      }
+      if ((++it & 63u) == 0) {
+        bool stop = *reinterpret_cast<volatile uint32_t*>(&h->abort) != 0;
+        if (!stop && clock64() - t0 > P.wait_bound) {
+          if (pending) record_timeout(P, kSiteProdEmpty, s);
+          stop = true;
+        }
+        if (__any_sync(0xffffffffu, stop)) return false;
+      }
+    }
+    return true;
   };
 
   auto issue_stats = [&](const Unit& u) -> bool {
@@ -288,8 +320,7 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
       const int pi = lane;
       const bool mine = pi < up;
       const uint32_t sq = seq + (uint32_t)pi;
-      if (!lane_acquire(mine, sq)) return false;
-      if (mine) {
+      const bool ok_i = lane_issue(mine, sq, [&]() {
         const int isd = pi >= npc;
         const int kp = u.c * kUnitPieces + (isd ? pi - npc : pi);
         const int ne = min(P.g.pe, V - kp * P.g.pe);
@@ -308,9 +339,9 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
         m.npc = npc;
         mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(ne * es));
         bulk_g2s(S.ring[slot], row + (size_t)kp * kPieceBytes, (uint32_t)(ne * es), &S.full[slot]);
-      }
+      });
       seq += (uint32_t)up;
-      return true;
+      return ok_i;
     }
     for (int pi = 0; pi < up; ++pi) {
       const int isd = pi >= npc;
@@ -368,8 +399,7 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
       const int pi = lane;
       const bool mine = pi < npc;
       const uint32_t sq = seq + (uint32_t)pi;
-      if (!lane_acquire(mine, sq)) return false;
-      if (mine) {
+      const bool ok_i = lane_issue(mine, sq, [&]() {
         const int kp = c * kUnitPieces + pi;
         const int ne = min(P.g.re, V - kp * P.g.re);
         const int slot = sq % NS;
@@ -383,9 +413,9 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
           bulk_g2s(S.ring[slot], trow + off, bytes, &S.full[slot]);
           if (drow) bulk_g2s(S.ring[slot] + kResidRowBytes, drow + off, bytes, &S.full[slot]);
         }
-      }
+      });
       seq += (uint32_t)npc;
-      return true;
+      return ok_i;
     }
     for (int pi = 0; pi < npc; ++pi) {
       const int kp = c * kUnitPieces + pi;
@@ -403,65 +433,86 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
 
   // Work loop.  Ready residual work (published by row finalisers) is taken
   // first -- its rows were just read and are still in L2 -- otherwise the next
-  // statistics ticket.  A claimed but not yet published queue entry is only
-  // waited for when no statistics ticket is left, so no producer ever blocks
-  // while holding statistics work.
+  // statistics ticket.  Every global round trip of the loop (the next ticket,
+  // the queue counters, a queue claim, the value of a claimed entry) is issued
+  // by lane 0 one iteration ahead and consumed in the next, so while
+  // statistics work remains the producer never stalls on a round trip.  A
+  // claimed entry that is not yet published is waited for only when no
+  // statistics ticket is left.
+  enum : int { kActStats = 0, kActResid = 1, kActWait = 2, kActClaim = 3, kActDone = 4 };
+  constexpr uint32_t kNone = 0xffffffffu;
   WsHeader* hq = h;
-  unsigned long long next = 0;  // prefetched statistics ticket
-  uint32_t v_head = 0, v_res = 0;  // last seen queue counters (loaded a unit ahead)
+  unsigned long long next = 0;     // prefetched statistics ticket
+  uint32_t v_head = 0, v_res = 0;  // queue counters seen one iteration ago
+  uint32_t claim = kNone;          // queue claim issued last iteration
+  unsigned long long ev = 0;       // entry[held] as loaded last iteration
+  long long held = -1;             // claimed queue entry not yet issued
   if (lane == 0) {
     next = atomicAdd(&h->ticket, 1ull);
     v_head = ld_relaxed_u32(&hq->rq_head);
     v_res = ld_relaxed_u32(&hq->rq_reserve);
   }
-  long long held = -1;  // claimed queue entry not yet issued
   while (ok) {
     if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
       ok = false;
       break;
     }
-    const unsigned long long t = __shfl_sync(0xffffffffu, next, 0);
-    const bool stats_left = (long long)t < P.tickets;
-    // try to claim residual work the counters say is published
-    if (held < 0) {
-      uint32_t claim = 0xffffffffu;
-      if (lane == 0) {
-        const bool avail = v_head < v_res;
-        if (avail || !stats_left) claim = atomicAdd(&hq->rq_head, 1u);
-        v_head = ld_relaxed_u32(&hq->rq_head);
-        v_res = ld_relaxed_u32(&hq->rq_reserve);
-      }
-      claim = __shfl_sync(0xffffffffu, claim, 0);
-      if (claim != 0xffffffffu) {
-        if (claim >= P.resid_units) {
-          if (!stats_left) break;  // every residual unit is claimed: done
-        } else {
+    int act = kActStats;
+    if (lane == 0) {
+      const bool stats_left = (long long)next < P.tickets;
+      if (claim != kNone) {  // resolve last iteration's claim
+        if (claim < P.resid_units) {
           held = claim;
+          ev = 0;  // its value is loaded below, for the next iteration
+        } else if (!stats_left) {
+          act = kActDone;  // every residual unit is claimed
         }
+        claim = kNone;
+      }
+      if (act != kActDone) {
+        if (held >= 0 && ev != 0)
+          act = kActResid;
+        else if (held >= 0 && !stats_left)
+          act = kActWait;
+        else if (stats_left)
+          act = kActStats;
+        else
+          act = kActClaim;
       }
     }
-    if (held >= 0) {
+    act = __shfl_sync(0xffffffffu, act, 0);
+    if (act == kActDone) break;
+    if (act == kActResid || act == kActWait) {
       unsigned long long e = 0;
       if (lane == 0) {
-        e = ld_acquire_u64(rq_of(P) + held);
-        if (!e && !stats_left) e = wait_entry(P, (unsigned)held);
+        // acquire: the row's stop record was written before the entry
+        e = (act == kActWait) ? wait_entry(P, (unsigned)held) : ld_acquire_u64(rq_of(P) + held);
+        if (e) rq_of(P)[held] = 0ull;  // self-reset for the next call
+        held = -1;
       }
       e = __shfl_sync(0xffffffffu, e, 0);
       __syncwarp();
-      if (e) {
-        if (lane == 0) rq_of(P)[held] = 0ull;  // self-reset for the next call
-        held = -1;
-        ok = issue_resid((int)(e >> 32) - 1, (int)(e & 0xffffffffu));
-        continue;
-      }
-      if (!stats_left) {  // the bounded wait ran out
+      if (!e) {  // the bounded wait ran out
         ok = false;
         break;
       }
-    }
-    if (stats_left) {
-      if (lane == 0) next = atomicAdd(&h->ticket, 1ull);  // prefetch the next ticket
+      ok = issue_resid((int)(e >> 32) - 1, (int)(e & 0xffffffffu));
+    } else if (act == kActStats) {
+      const unsigned long long t = __shfl_sync(0xffffffffu, next, 0);
+      if (lane == 0) next = atomicAdd(&h->ticket, 1ull);  // next ticket, used next iteration
       ok = issue_stats(decode_ticket((long long)t, P));
+    } else {  // kActClaim: no statistics left; the claim resolves next iteration
+      if (lane == 0) claim = atomicAdd(&hq->rq_head, 1u);
+    }
+    // round trips for the next iteration
+    if (lane == 0) {
+      if (held >= 0) {
+        ev = ld_relaxed_u64(rq_of(P) + held);
+      } else if (claim == kNone && v_head < v_res && (long long)next < P.tickets) {
+        claim = atomicAdd(&hq->rq_head, 1u);  // published work is waiting: claim one
+      }
+      v_head = ld_relaxed_u32(&hq->rq_head);
+      v_res = ld_relaxed_u32(&hq->rq_reserve);
     }
   }
   // one end marker per consumer warp (lane w marks the stage consumer w takes next)
@@ -616,82 +667,117 @@ __device__ __forceinline__ float resid_piece(const unsigned char* slot, const St
 // hand-offs: position -> row -> residual -> token
 // ---------------------------------------------------------------------------
 // Last statistics unit of row b: combine every position's unit partials, run
-// all accept tests (lane j = position j, in fp64), find the first rejection n
-// and publish the stop constants.  One fence, one release.
-__device__ void finalize_row(const DenseParams& P, int b, int lane) {
-  __threadfence();
+// all accept tests (lane j = position j), find the first rejection n
+// and publish the stop constants.  The row's partials are staged through a
+// 4 KB shared-memory scratch with one cooperative load per round, so the
+// whole hand-off costs a few global round trips.
+constexpr int kFinScratch = 128;  // unit partials (4 KB)
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void combine_part(const UnitPart& u, float& Ct, ff& St, float& Cd,
+                                             ff& Sd) {
+  const ff ut{u.St_hi, u.St_lo}, ud{u.Sd_hi, u.Sd_lo};
+  if (u.ct > Ct) {
+    St = ff_add(ff_mul_f(St, part_scale(Ct, u.ct)), ut);
+    Ct = u.ct;
+  } else {
+    St = ff_add(St, ff_mul_f(ut, part_scale(u.ct, Ct)));
+  }
+  if (u.cd > Cd) {
+    Sd = ff_add(ff_mul_f(Sd, part_scale(Cd, u.cd)), ud);
+    Cd = u.cd;
+  } else {
+    Sd = ff_add(Sd, ff_mul_f(ud, part_scale(u.cd, Cd)));
+  }
+}
+
+__device__ void finalize_row(const DenseParams& P, int b, int lane, UnitPart* scr) {
+  fence_acq_rel_gpu();
   const int G = P.G, nc = P.g.nc_s;
-  const UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
+  UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
+  // reserve the row's queue entries now; the result is needed only at the end
+  unsigned base = 0;
+  if (lane == 0) base = atomicAdd(&hdr_of(P)->rq_reserve, (unsigned)P.g.nc_r);
   int n = G, err_any = 0, have_stop = 0;
-  float s_ct = 0.f, s_cd = 0.f;
-  double s_St = 1.0, s_Sd = 1.0;
+  float s_ct = 0.f, s_cd = 0.f, s_St = 1.f, s_Sd = 1.f;
   for (int j0 = 0; j0 <= G; j0 += 32) {
     const int j = j0 + lane;
     const bool on = j <= G;
+    const int npos = min(32, G + 1 - j0);
     int err = 0, x = 0;
-    float tx = 0.f, dx = 0.f;
+    float uacc = 0.f;
     if (on && j < G) {
       x = P.x[(size_t)b * G + j];
-      if (x < 0 || x >= P.V) {
-        err = 1;
-      } else {
-        tx = load_logit(target_row(P, b, j), x, P.bf16);
-        dx = load_logit(draft_row(P, b, j), x, P.bf16);
-      }
+      uacc = P.u_acc[(size_t)b * G + j];
     }
-    // online combination of the position's unit partials
     float Ct = -INFINITY, Cd = -INFINITY;
-    double St = 0.0, Sd = 0.0;
-    if (on) {
-      const UnitPart* up = up_row + (size_t)j * nc;
-      for (int k0 = 0; k0 < nc; k0 += 4) {
-        UnitPart buf[4];
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-          if (k0 + kk < nc) {
-            buf[kk] = ldcg32(up + k0 + kk);
+    ff St{0.f, 0.f}, Sd{0.f, 0.f};
+    const int kstep = max(1, kFinScratch / npos);
+    bool gathered = false;
+    float tx = 0.f, dx = 0.f;
+    for (int k0 = 0; k0 < nc; k0 += kstep) {
+      const int kn = min(kstep, nc - k0);
+      const int total = npos * kn;  // <= kFinScratch
+      // cooperative copy of this round's partials into the scratch: every
+      // copy in flight at once (cp.async, no registers), then zero the source
+      __syncwarp();  // the previous round's reads of the scratch are done
+      for (int f = lane; f < total; f += 32) {
+        const int pp = f / kn, kk = f - pp * kn;
+        const unsigned char* q =
+            reinterpret_cast<const unsigned char*>(up_row + (size_t)(j0 + pp) * nc + k0 + kk);
+        cp_async16(scr + f, q);
+        cp_async16(reinterpret_cast<unsigned char*>(scr + f) + 16, q + 16);
+      }
+      if (!gathered) {  // the gather at the draft token, overlapping the copies
+        gathered = true;
+        if (on && j < G) {
+          if (x < 0 || x >= P.V) {
+            err = 1;
           } else {
-            buf[kk].St = buf[kk].Sd = 0.0;
-            buf[kk].ct = buf[kk].cd = -INFINITY;
+            tx = load_logit(target_row(P, b, j), x, P.bf16);
+            dx = load_logit(draft_row(P, b, j), x, P.bf16);
           }
         }
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-        const UnitPart& u = buf[kk];
-        if (u.ct > Ct) {
-          St = St * (double)part_scale(Ct, u.ct) + u.St;
-          Ct = u.ct;
-        } else {
-          St += u.St * (double)part_scale(u.ct, Ct);
-        }
-        if (u.cd > Cd) {
-          Sd = Sd * (double)part_scale(Cd, u.cd) + u.Sd;
-          Cd = u.cd;
-        } else {
-          Sd += u.Sd * (double)part_scale(u.cd, Cd);
-        }
-        }
       }
-      err |= !(Ct > -INFINITY && Ct < INFINITY && St > 0.0 && St < INFINITY);
-      if (j < G) err |= !(Cd > -INFINITY && Cd < INFINITY && Sd > 0.0 && Sd < INFINITY);
-      // consumed: leave the workspace zero for the next call
-      for (int k = 0; k < nc; ++k) {
-        int4* q = reinterpret_cast<int4*>(const_cast<UnitPart*>(up + k));
+      cp_async_wait_all();
+      for (int f = lane; f < total; f += 32) {  // consumed: leave the workspace zero
+        const int pp = f / kn, kk = f - pp * kn;
+        int4* q = reinterpret_cast<int4*>(up_row + (size_t)(j0 + pp) * nc + k0 + kk);
         q[0] = make_int4(0, 0, 0, 0);
         q[1] = make_int4(0, 0, 0, 0);
       }
+      __syncwarp();
+      if (on)
+        for (int k = 0; k < kn; ++k) combine_part(scr[lane * kn + k], Ct, St, Cd, Sd);
+    }
+    const float Stf = ff_to_f(St), Sdf = ff_to_f(Sd);
+    if (on) {
+      err |= !(Ct > -INFINITY && Ct < INFINITY && Stf > 0.f && Stf < INFINITY);
+      if (j < G) err |= !(Cd > -INFINITY && Cd < INFINITY && Sdf > 0.f && Sdf < INFINITY);
     }
     int acc = 1;
-    double a = 0.0;
+    float a = 0.f;
     if (on && j < G && !err) {
-      const double L = (double)kLog2e;
-      const double p = (tx == -INFINITY) ? 0.0 : exp2((double)tx * L - (double)Ct) / St;
-      const double q = (dx == -INFINITY) ? 0.0 : exp2((double)dx * L - (double)Cd) / Sd;
-      const double ratio = (q > 0.0) ? p / q : 0.0;
-      a = ratio < 1.0 ? ratio : 1.0;
-      acc = (double)P.u_acc[(size_t)b * G + j] < a;
+      // p/q = 2^((tx L - Ct) - (dx L - Cd)) * (Sd / St); the exponent is formed
+      // exactly (two-product) and rounded once
+      float ratio = 0.f;
+      if (tx > -INFINITY && dx > -INFINITY) {
+        const ff ea = ff_add_f(two_prod(tx, kLog2e), -Ct);
+        const ff ed = ff_add_f(two_prod(dx, kLog2e), -Cd);
+        ratio = exp2f(ff_to_f(ff_sub(ea, ed))) * __fdiv_rn(Sdf, Stf);
+      }
+      a = fminf(ratio, 1.f);
+      acc = uacc < a;
     }
-    if (on && j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : (float)a;
+    if (on && j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
     err_any |= __any_sync(0xffffffffu, on && err);
     const unsigned rej = __ballot_sync(0xffffffffu, on && j < G && !acc);
     int src = -1;
@@ -705,8 +791,8 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane) {
       have_stop = 1;
       s_ct = __shfl_sync(0xffffffffu, Ct, src);
       s_cd = __shfl_sync(0xffffffffu, Cd, src);
-      s_St = __shfl_sync(0xffffffffu, St, src);
-      s_Sd = __shfl_sync(0xffffffffu, Sd, src);
+      s_St = __shfl_sync(0xffffffffu, Stf, src);
+      s_Sd = __shfl_sync(0xffffffffu, Sdf, src);
     }
   }
   if (lane == 0) {
@@ -721,22 +807,20 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane) {
       st.mode = 0;
       st.ct = s_ct;
       st.cd = s_cd;
-      st.invSt = (float)(1.0 / s_St);
-      st.invSd = (float)(1.0 / s_Sd);
+      st.invSt = __fdiv_rn(1.f, s_St);
+      st.invSd = __fdiv_rn(1.f, s_Sd);
     } else {
       st.mode = 1;
       st.ct = s_ct;
       st.cd = 0.f;
-      st.invSt = (float)(1.0 / s_St);
+      st.invSt = __fdiv_rn(1.f, s_St);
       st.invSd = 0.f;
     }
     ws_at<StopInfo>(P, P.L.stop)[b] = st;
     ws_at<uint32_t>(P, P.L.cnt_row)[b] = 0;
-    __threadfence();
+    fence_acq_rel_gpu();
   }
   // publish the row's residual units to the queue
-  unsigned base = 0;
-  if (lane == 0) base = atomicAdd(&hdr_of(P)->rq_reserve, (unsigned)P.g.nc_r);
   base = __shfl_sync(0xffffffffu, base, 0);
   __syncwarp();
   for (int c = lane; c < P.g.nc_r; c += 32)
@@ -744,172 +828,178 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane) {
   __syncwarp();
 }
 
-// The residual (or p) values of one residual piece for the final walk: lane l
-// holds the piece's elements [l*per, (l+1)*per) in ascending order, loaded
-// with 16-byte vectors when the rows are aligned.  Values are bit-identical
-// to those resid_piece summed.
+// Select the token of row b from its per-piece masses (float-float prefix over
+// pieces, then over the fp32 element values of the chosen piece).  The
+// masses, then the chosen piece's logits, are staged in the shared scratch
+// with cp.async: two global round trips.
 template <int BF16>
-__device__ __forceinline__ void piece_values(const DenseParams& P, const unsigned char* trow,
-                                             const unsigned char* drow, int y0, int ne,
-                                             const StopInfo& st, int lane, float (&rv)[32]) {
-  constexpr int per = BF16 ? 32 : 16;  // elements per lane (64 bytes)
-  const int e0 = lane * per;
-  if (P.aligned && e0 + per <= ne) {
-    const uint4* tv = reinterpret_cast<const uint4*>(trow + (size_t)(y0 + e0) * (BF16 ? 2 : 4));
-    const uint4* dv = drow ? reinterpret_cast<const uint4*>(drow + (size_t)(y0 + e0) * (BF16 ? 2 : 4))
-                           : nullptr;
-    uint4 t4[4], d4[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      t4[i] = __ldcg(tv + i);
-      d4[i] = dv ? __ldcg(dv + i) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const uint32_t* tw = reinterpret_cast<const uint32_t*>(&t4[i]);
-      const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d4[i]);
-      if (BF16) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float t = (e & 1) ? bf16_hi(tw[e >> 1]) : bf16_lo(tw[e >> 1]);
-          const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
-          rv[i * 8 + e] = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          rv[i * 4 + e] = resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), st.ct, st.cd,
-                                    st.invSt, st.invSd, st.mode);
-      }
-    }
-#pragma unroll
-    for (int e = per; e < 32; ++e) rv[e] = 0.f;
+__device__ __forceinline__ float piece_val(const float* tsm, const float* dsm, int e,
+                                           const StopInfo& st) {
+  float t, d;
+  if (BF16) {
+    t = bf16_to_f32(reinterpret_cast<const uint16_t*>(tsm)[e]);
+    d = bf16_to_f32(reinterpret_cast<const uint16_t*>(dsm)[e]);
   } else {
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      const int y = e0 + e;
-      float r = 0.f;
-      if (e < per && y < ne) {
-        const float t = load_logit(trow, y0 + y, BF16);
-        const float d = drow ? load_logit(drow, y0 + y, BF16) : 0.f;
-        r = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
-      }
-      rv[e] = r;
-    }
+    t = tsm[e];
+    d = dsm[e];
   }
+  return resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
 }
 
-// Select the token of row b from its per-piece masses (fp64 prefix over
-// pieces, then over the fp32 element values of the chosen piece).
 template <int BF16>
-__device__ void final_select(const DenseParams& P, int b, int lane) {
-  __threadfence();
+__device__ void final_select(const DenseParams& P, int b, int lane, float* scr) {
+  fence_acq_rel_gpu();
   const int G = P.G, V = P.V, np = P.g.np_r, re = P.g.re;
   StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
-  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
-  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * np;
-  const int n = st.n;
   const float us = P.u_s[b];
+  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
+  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np_r4;
+  const int n = st.n;
   int y = -1;
-  double T = 0.0;
+  ff T{0.f, 0.f};
+  constexpr int kScrFloats = 1024;  // 4 KB
   if (st.mode != 2) {
     const unsigned char* trow = target_row(P, b, n);
     const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, n) : nullptr;
+    const bool staged = np <= kScrFloats;
+    if (staged) {
+      for (int k = lane * 4; k < np; k += 128) cp_async16(scr + k, rm + k);
+      cp_async_wait_all();
+    }
+    __syncwarp();
+    const float* mv = staged ? scr : rm;
     const int per = (np + 31) / 32;
     const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
-    double ls = 0.0;
-    for (int k = k0; k < k1; ++k) ls += (double)__ldcg(rm + k);
-    double ex = warp_exclusive_scan_d(ls, lane);
-    T = __shfl_sync(0xffffffffu, ex + ls, 31);
-    if (!(T > 0.0) && st.mode == 0) {
+    ff ls{0.f, 0.f};
+    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, mv[k]);
+    ff ex = warp_exclusive_scan_ff(ls, lane);
+    T = ff_shfl(ff_add(ex, ls), 31);
+    if (!(T.hi > 0.f) && st.mode == 0) {
       // zero residual after a rejection (only through rounding): draw from p_n
       st.mode = 1;
       drow = nullptr;
       for (int k = 0; k < np; ++k) {
         const int y0 = k * re, ne = min(re, V - y0);
-        float s = 0.f;
+        float sum = 0.f;
         for (int e = lane; e < ne; e += 32)
-          s += resid_val(load_logit(trow, y0 + e, BF16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
-        s = warp_sum(s);
-        if (lane == 0) rm[k] = s;
+          sum += resid_val(load_logit(trow, y0 + e, BF16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
+        sum = warp_sum(sum);
+        if (lane == 0) {
+          if (staged)
+            scr[k] = sum;
+          else
+            rm[k] = sum;
+        }
       }
-      __threadfence();
+      fence_acq_rel_gpu();
       __syncwarp();
-      ls = 0.0;
-      for (int k = k0; k < k1; ++k) ls += (double)__ldcg(rm + k);
-      ex = warp_exclusive_scan_d(ls, lane);
-      T = __shfl_sync(0xffffffffu, ex + ls, 31);
+      ls = ff{0.f, 0.f};
+      for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, staged ? scr[k] : __ldcg(rm + k));
+      ex = warp_exclusive_scan_ff(ls, lane);
+      T = ff_shfl(ff_add(ex, ls), 31);
     }
-    const double target = (double)us * T;
+    const ff target = ff_mul_f(T, us);
     // piece level
-    const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && (ex + ls > target));
+    const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && ff_gt(ff_add(ex, ls), target));
     int kstar = -1;
-    double base = 0.0;
+    ff base{0.f, 0.f};
     bool clamp = false;
     if (hit) {
       const int fl = __ffs(hit) - 1;
       if (lane == fl) {
-        double acc = ex;
+        ff acc = ex;
+        ff prev = ex;
         for (int k = k0; k < k1; ++k) {
-          const double mk = (double)__ldcg(rm + k);
-          if (acc + mk > target) {
+          prev = acc;
+          acc = ff_add_f(acc, staged ? scr[k] : __ldcg(rm + k));
+          if (ff_gt(acc, target)) {
             kstar = k;
-            base = acc;
+            base = prev;
             break;
           }
-          acc += mk;
         }
         if (kstar < 0) {  // rounding between the two sums: last piece of the lane
           kstar = k1 - 1;
-          base = acc - (double)__ldcg(rm + kstar);
+          base = prev;
         }
       }
       kstar = __shfl_sync(0xffffffffu, kstar, fl);
-      base = __shfl_sync(0xffffffffu, base, fl);
+      base = ff_shfl(base, fl);
     } else {
       clamp = true;  // u*T at or past the total: last piece with mass
       int last = -1;
       for (int k = k0; k < k1; ++k)
-        if (__ldcg(rm + k) > 0.f) last = k;
+        if ((staged ? scr[k] : __ldcg(rm + k)) > 0.f) last = k;
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
       kstar = last < 0 ? 0 : last;
     }
     // the masses are consumed: leave the workspace zero for the next call
-    for (int k = k0; k < k1; ++k) rm[k] = 0.f;
-    // element level within piece kstar (values in registers)
+    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
+    __syncwarp();
+    // element level within piece kstar: stage its target and draft slices
     const int y0 = kstar * re, ne = min(re, V - y0);
-    constexpr int per_lane = BF16 ? 32 : 16;
-    float rv[32];
-    piece_values<BF16>(P, trow, drow, y0, ne, st, lane, rv);
-    double es = 0.0;
-    int lastpos = -1;
-#pragma unroll
-    for (int e = 0; e < 32; ++e) {
-      es += (double)rv[e];
-      if (rv[e] > 0.f) lastpos = lane * per_lane + e;
+    const float* tsm = scr;
+    const float* dsm = scr + 512;  // 2 KB in
+    if (P.aligned) {
+      const int nchunk = (ne * (BF16 ? 2 : 4)) / 16;  // whole 16-byte chunks (rows are aligned)
+      const unsigned char* ts = trow + (size_t)y0 * (BF16 ? 2 : 4);
+      const unsigned char* ds = drow ? drow + (size_t)y0 * (BF16 ? 2 : 4) : nullptr;
+      for (int c = lane; c < nchunk; c += 32) {
+        cp_async16(reinterpret_cast<unsigned char*>(scr) + 16 * c, ts + 16 * c);
+        if (ds) cp_async16(reinterpret_cast<unsigned char*>(scr + 512) + 16 * c, ds + 16 * c);
+      }
+      cp_async_wait_all();
+    } else {
+      for (int e = lane; e < ne; e += 32) {
+        if (BF16) {
+          reinterpret_cast<uint16_t*>(scr)[e] = reinterpret_cast<const uint16_t*>(trow)[y0 + e];
+          if (drow) reinterpret_cast<uint16_t*>(scr + 512)[e] = reinterpret_cast<const uint16_t*>(drow)[y0 + e];
+        } else {
+          scr[e] = reinterpret_cast<const float*>(trow)[y0 + e];
+          if (drow) scr[512 + e] = reinterpret_cast<const float*>(drow)[y0 + e];
+        }
+      }
     }
-    const double eex = warp_exclusive_scan_d(es, lane);
-    const double tl = target - base;
-    const unsigned ehit = clamp ? 0u : __ballot_sync(0xffffffffu, eex + es > tl);
+    if (!drow) {  // bonus / fallback: the draft slice is unused; keep it finite
+      for (int e = lane; e < 512; e += 32) scr[512 + e] = 0.f;
+    }
+    __syncwarp();
+    const int q = (ne + 31) / 32;
+    const int e0 = min(ne, lane * q), e1 = min(ne, e0 + q);
+    ff es{0.f, 0.f};
+    int lastpos = -1;
+    for (int e = e0; e < e1; ++e) {
+      const float r = piece_val<BF16>(tsm, dsm, e, st);
+      es = ff_add_f(es, r);
+      if (r > 0.f) lastpos = e;
+    }
+    const ff eex = warp_exclusive_scan_ff(es, lane);
+    const ff tl = ff_sub(target, base);
+    const unsigned ehit =
+        clamp ? 0u : __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(eex, es), tl));
     if (ehit) {
       const int fl = __ffs(ehit) - 1;
       int yy = -1;
-      double acc = base + eex;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        acc += (double)rv[e];
-        if (yy < 0 && acc > target) yy = lane * per_lane + e;
+      if (lane == fl) {
+        ff acc = ff_add(base, eex);
+        for (int e = e0; e < e1; ++e) {
+          acc = ff_add_f(acc, piece_val<BF16>(tsm, dsm, e, st));
+          if (ff_gt(acc, target)) {
+            yy = e;
+            break;
+          }
+        }
+        if (yy < 0) yy = lastpos >= 0 ? lastpos : e1 - 1;
       }
-      if (yy < 0) yy = lastpos;
-      y = __shfl_sync(0xffffffffu, yy, fl);
-      if (y < 0) y = 0;
-      y += y0;
+      y = y0 + __shfl_sync(0xffffffffu, yy, fl);
     } else {
       int lp = lastpos;
       for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
       y = y0 + (lp < 0 ? 0 : lp);
     }
   }
+  if (st.mode == 2)  // an error row never reached the piece-level search
+    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
   // outputs
   const int nn = (st.mode == 2) ? -1 : n;
   for (int j = lane; j <= G; j += 32) {
@@ -917,18 +1007,16 @@ __device__ void final_select(const DenseParams& P, int b, int lane) {
     if (nn >= 0) v = (j < nn) ? P.x[(size_t)b * G + j] : (j == nn ? y : -1);
     tok[j] = v;
   }
-  if (st.mode == 2)  // an error row never reached the piece-level search
-    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
   if (lane == 0) {
     P.n_out[b] = nn;
     StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
     if (P.keep_stop) {  // read (and cleared) by the residual-output kernel
       sp->mode = st.mode;
-      sp->T = T;
+      sp->T = (double)T.hi + (double)T.lo;
     } else {
-      int4* q = reinterpret_cast<int4*>(sp);
-      q[0] = make_int4(0, 0, 0, 0);
-      q[1] = make_int4(0, 0, 0, 0);
+      int4* qq = reinterpret_cast<int4*>(sp);
+      qq[0] = make_int4(0, 0, 0, 0);
+      qq[1] = make_int4(0, 0, 0, 0);
     }
     ws_at<uint32_t>(P, P.L.cnt_res)[b] = 0;
   }
@@ -992,20 +1080,22 @@ __device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane
         const float sl = have ? U.s[lane] : 0.f;
         const float Ct = warp_max((have && !isd) ? cl : -INFINITY);
         const float Cd = warp_max((have && isd) ? cl : -INFINITY);
-        const double wt = (have && !isd) ? (double)sl * (double)part_scale(cl, Ct) : 0.0;
-        const double wd = (have && isd) ? (double)sl * (double)part_scale(cl, Cd) : 0.0;
-        const double St = warp_sum_d(wt), Sd = warp_sum_d(wd);
+        const ff wt = (have && !isd) ? two_prod(sl, part_scale(cl, Ct)) : ff{0.f, 0.f};
+        const ff wd = (have && isd) ? two_prod(sl, part_scale(cl, Cd)) : ff{0.f, 0.f};
+        const ff St = warp_sum_ff(wt), Sd = warp_sum_ff(wd);
         if (lane == 0) {
           U.count = 0;
           mbar_arrive(&S.ufree[m.uslot]);
           UnitPart u;
-          u.St = St;
-          u.Sd = Sd;
+          u.St_hi = St.hi;
+          u.St_lo = St.lo;
+          u.Sd_hi = Sd.hi;
+          u.Sd_lo = Sd.lo;
           u.ct = Ct;
           u.cd = Cd;
           u.pad[0] = u.pad[1] = 0.f;
           ws_at<UnitPart>(P, P.L.upart)[((size_t)m.b * (G + 1) + m.j) * P.g.nc_s + m.unit_c] = u;
-          __threadfence();
+          fence_acq_rel_gpu();
           const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + m.b, 1u);
           row_done = (o2 == (unsigned)((G + 1) * P.g.nc_s) - 1);
         }
@@ -1025,11 +1115,11 @@ __device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane
       int row_done = 0;
       if (lane == 0 && old == (unsigned)m.upieces - 1) {
         __threadfence_block();
-        float* rm = ws_at<float>(P, P.L.rmass) + (size_t)m.b * P.g.np_r + m.unit_c * kUnitPieces;
+        float* rm = ws_at<float>(P, P.L.rmass) + (size_t)m.b * P.g.np_r4 + m.unit_c * kUnitPieces;
         for (int k = 0; k < m.upieces; ++k) rm[k] = U.s[k];
         U.count = 0;
         mbar_arrive(&S.ufree[m.uslot]);
-        __threadfence();
+        fence_acq_rel_gpu();
         const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_res) + m.b, 1u);
         row_done = (o2 == (unsigned)P.g.nc_r - 1);
       }
@@ -1069,7 +1159,7 @@ __device__ void finaliser(const DenseParams& P, Smem<NS, NW>& S, int lane) {
         record_timeout(P, kSiteFinIdle, head);
         state = 3;
       } else {
-        nanosleep_ns(32);
+        nanosleep_ns(256);
       }
     }
     state = __shfl_sync(0xffffffffu, state, 0);
@@ -1078,11 +1168,11 @@ __device__ void finaliser(const DenseParams& P, Smem<NS, NW>& S, int lane) {
     item = __shfl_sync(0xffffffffu, item, 0);
     __syncwarp();
     if (item > 0) {
-      finalize_row(P, item - 1, lane);
+      finalize_row(P, item - 1, lane, S.fin_scratch);
     } else if (P.bf16) {
-      final_select<1>(P, -item - 1, lane);
+      final_select<1>(P, -item - 1, lane, reinterpret_cast<float*>(S.fin_scratch));
     } else {
-      final_select<0>(P, -item - 1, lane);
+      final_select<0>(P, -item - 1, lane, reinterpret_cast<float*>(S.fin_scratch));
     }
     ++head;
     if (lane == 0) *reinterpret_cast<volatile unsigned*>(&S.fin_head) = head;
@@ -1130,7 +1220,7 @@ __global__ void __maxnreg__((dense_regs<NW, CTAS>()))
   __syncthreads();
   if (threadIdx.x == 0) {
     WsHeader* h = hdr_of(P);
-    __threadfence();
+    fence_acq_rel_gpu();
     const unsigned prev = atomicAdd(&h->exit_cnt, 1u);
     // after a timeout the counters are left as they are, for diagnosis
     if (prev == gridDim.x - 1 && !*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
@@ -1138,7 +1228,7 @@ __global__ void __maxnreg__((dense_regs<NW, CTAS>()))
       h->rq_head = 0u;
       h->rq_reserve = 0u;
       h->exit_cnt = 0u;
-      __threadfence();
+      fence_acq_rel_gpu();
     }
   }
 }
@@ -1162,11 +1252,11 @@ __global__ void dense_resid_out_kernel(const __grid_constant__ DenseParams P, fl
   }
   const unsigned char* trow = target_row(P, b, st.n);
   const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
-  const double invT = 1.0 / st.T;
+  const float invT = __fdiv_rn(1.f, (float)st.T);
   for (int y = threadIdx.x; y < P.V; y += blockDim.x) {
     const float t = load_logit(trow, y, P.bf16);
     const float d = drow ? load_logit(drow, y, P.bf16) : 0.f;
-    o[y] = (float)((double)resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode) * invT);
+    o[y] = resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode) * invT;
   }
 }
 

@@ -39,6 +39,7 @@ struct DenseGeom {
   int re;    // elements per residual piece (per row)
   int np_s;  // statistics pieces per row
   int np_r;  // residual pieces per row
+  int np_r4; // np_r rounded up to a multiple of 4 (16-byte aligned rows of masses)
   int nc_s;  // statistics units per (row, position)
   int nc_r;  // residual units per row
 };
@@ -50,6 +51,7 @@ inline DenseGeom dense_geom(int V, int es) {
   g.re = kResidRowBytes / es;
   g.np_s = (V + g.pe - 1) / g.pe;
   g.np_r = (V + g.re - 1) / g.re;
+  g.np_r4 = (g.np_r + 3) / 4 * 4;
   g.nc_s = (g.np_s + kUnitPieces - 1) / kUnitPieces;
   g.nc_r = (g.np_r + kUnitPieces - 1) / kUnitPieces;
   return g;
@@ -58,7 +60,7 @@ inline DenseGeom dense_geom(int V, int es) {
 // Combined statistics of one work unit (up to 8 target + 8 draft pieces):
 // S = sum 2^(v*log2e - c) over the unit's elements, c = log2e * (max logit).
 struct UnitPart {
-  double St, Sd;
+  float St_hi, St_lo, Sd_hi, Sd_lo;  // float-float sums
   float ct, cd;
   float pad[2];
 };
@@ -94,7 +96,7 @@ inline DenseLayout dense_layout(long long B, int G, const DenseGeom& g) {
   L.stop = o;
   o = align_up(o + sizeof(StopInfo) * (size_t)B, 256);
   L.rmass = o;
-  o = align_up(o + sizeof(float) * (size_t)B * (size_t)g.np_r, 256);
+  o = align_up(o + sizeof(float) * (size_t)B * (size_t)g.np_r4, 256);
   L.total = o;
   return L;
 }

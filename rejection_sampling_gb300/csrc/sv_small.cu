@@ -5,7 +5,7 @@
 // read position i's row with no bank conflicts; lane i owns position i:
 // softmax statistics of its target and draft rows, the gather at its draft
 // token and its accept test.  A ballot gives the first rejection; the whole
-// warp then draws the replacement (or the bonus token) by an fp64 prefix over
+// warp then draws the replacement (or the bonus token) by a float-float prefix over
 // the fp32 residual values in ascending id order.
 //
 //  dense     : positions 0..gamma; target rows 0..gamma, draft rows 0..gamma-1;
@@ -113,10 +113,10 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
         const float tx = st[lane * VS + x], dx = sd[lane * VS + x];
         float ratio = 0.f;
         if (tx > -INFINITY && dx > -INFINITY) {
-          // log2 p(x) - log2 q(x) in fp64 (exact products), then one fp32 exp2
-          const double L = (double)kLog2e;
-          const double dl = ((double)tx * L - (double)ct) - ((double)dx * L - (double)cd);
-          ratio = exp2f((float)dl) * (Sd / St);
+          // log2 p(x) - log2 q(x) formed exactly (two-product), rounded once
+          const ff ea = ff_add_f(two_prod(tx, kLog2e), -ct);
+          const ff ed = ff_add_f(two_prod(dx, kLog2e), -cd);
+          ratio = exp2f(ff_to_f(ff_sub(ea, ed))) * __fdiv_rn(Sd, St);
         }
         a = fminf(ratio, 1.f);
         acc = P.u_acc[(size_t)b * NT + lane] < a;
@@ -131,7 +131,7 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   // ---- draw at the stop position ----
   int y = -1;
   int mode = 2;  // 0 residual, 1 p only, 2 none
-  double T = 0.0;
+  ff T{0.f, 0.f};
   float sct = 0.f, scd = 0.f, sist = 0.f, sisd = 0.f;
   int srow = 0;
   if (n >= 0 && (n < NT || !P.anyorder)) {
@@ -146,26 +146,26 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
     const float* tr = st + srow * VS;
     const float* dr = sd + srow * VS;
     for (int attempt = 0; attempt < 2; ++attempt) {
-      double ls = 0.0;
-      for (int e = e0; e < e1; ++e) ls += (double)resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode);
-      const double ex = warp_exclusive_scan_d(ls, lane);
-      T = __shfl_sync(0xffffffffu, ex + ls, 31);
-      if (!(T > 0.0) && mode == 0) {  // zero residual through rounding: draw from p_n
+      ff ls{0.f, 0.f};
+      for (int e = e0; e < e1; ++e) ls = ff_add_f(ls, resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode));
+      const ff ex = warp_exclusive_scan_ff(ls, lane);
+      T = ff_shfl(ff_add(ex, ls), 31);
+      if (!(T.hi > 0.f) && mode == 0) {  // zero residual through rounding: draw from p_n
         mode = 1;
         continue;
       }
-      const double target = (double)P.u_s[b] * T;
-      const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && (ex + ls > target));
+      const ff target = ff_mul_f(T, P.u_s[b]);
+      const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(ex, ls), target));
       if (hit) {
         const int fl = __ffs(hit) - 1;
         if (lane == fl) {
-          double accm = ex;
+          ff accm = ex;
           int lastpos = -1;
           for (int e = e0; e < e1; ++e) {
             const float r = resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode);
             if (r > 0.f) lastpos = e;
-            accm += (double)r;
-            if (accm > target) {
+            accm = ff_add_f(accm, r);
+            if (ff_gt(accm, target)) {
               y = e;
               break;
             }
@@ -204,12 +204,12 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   }
   if (P.resid_out) {
     float* o = P.resid_out + (size_t)b * V;
-    const bool have = (mode != 2) && (T > 0.0);
-    const double invT = have ? 1.0 / T : 0.0;
+    const bool have = (mode != 2) && (T.hi > 0.f);
+    const float invT = have ? __fdiv_rn(1.f, ff_to_f(T)) : 0.f;
     const float* tr = st + srow * VS;
     const float* dr = sd + srow * VS;
     for (int e = lane; e < V; e += 32)
-      o[e] = have ? (float)((double)resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode) * invT) : 0.f;
+      o[e] = have ? resid_val(tr[e], dr[e], sct, scd, sist, sisd, mode) * invT : 0.f;
   }
 }
 

@@ -13,7 +13,7 @@
 // One CTA per row, one warp per position (gamma + 1 <= 32 warps).  Warp j
 // validates its lists and runs its accept test; a shared-memory scan finds
 // the first rejection n; warp n then merges its target list against the
-// sorted draft list (binary search per target id), scans the residual in fp64
+// sorted draft list (binary search per target id), scans the residual in float-float
 // in list order and draws the token.
 #include "sv_common.cuh"
 
@@ -118,32 +118,32 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
     const float r = __fsub_rn(p, list_lookup(did, dp, kd, tid[i]));
     return r > 0.f ? r : 0.f;
   };
-  double T = 0.0, ls = 0.0, ex = 0.0;
+  ff T{0.f, 0.f}, ls{0.f, 0.f}, ex{0.f, 0.f};
   for (int attempt = 0; attempt < 2; ++attempt) {
-    ls = 0.0;
-    for (int i = e0; i < e1; ++i) ls += (double)weight(i);
-    ex = warp_exclusive_scan_d(ls, lane);
-    T = __shfl_sync(0xffffffffu, ex + ls, 31);
-    if (!(T > 0.0) && mode == 0) {
+    ls = ff{0.f, 0.f};
+    for (int i = e0; i < e1; ++i) ls = ff_add_f(ls, weight(i));
+    ex = warp_exclusive_scan_ff(ls, lane);
+    T = ff_shfl(ff_add(ex, ls), 31);
+    if (!(T.hi > 0.f) && mode == 0) {
       mode = 1;  // zero residual through rounding: draw from the target list
       continue;
     }
     break;
   }
   int yi = -1;
-  if (T > 0.0) {
-    const double target = (double)P.u_s[b] * T;
-    const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && (ex + ls > target));
+  if (T.hi > 0.f) {
+    const ff target = ff_mul_f(T, P.u_s[b]);
+    const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(ex, ls), target));
     if (hit) {
       const int fl = __ffs(hit) - 1;
       if (lane == fl) {
-        double accm = ex;
+        ff accm = ex;
         int lastpos = -1;
         for (int i = e0; i < e1; ++i) {
           const float w = weight(i);
           if (w > 0.f) lastpos = i;
-          accm += (double)w;
-          if (accm > target) {
+          accm = ff_add_f(accm, w);
+          if (ff_gt(accm, target)) {
             yi = i;
             break;
           }
@@ -163,9 +163,8 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   for (int i = lane; i <= G; i += 32) tok[i] = (i < n) ? P.x[(size_t)b * G + i] : (i == n ? y : -1);
   if (lane == 0) P.n_out[b] = n;
   if (P.resid_out) {
-    const double invT = (T > 0.0) ? 1.0 / T : 0.0;
-    for (int i = lane; i < kt; i += 32)
-      P.resid_out[(size_t)b * kt + i] = (float)((double)weight(i) * invT);
+    const float invT = (T.hi > 0.f) ? __fdiv_rn(1.f, ff_to_f(T)) : 0.f;
+    for (int i = lane; i < kt; i += 32) P.resid_out[(size_t)b * kt + i] = weight(i) * invT;
   }
 }
 
