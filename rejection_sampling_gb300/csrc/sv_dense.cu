@@ -294,7 +294,7 @@ __device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
     const long long t0 = clock64();
     unsigned it = 0;
     while (__any_sync(0xffffffffu, pending)) {
-      if (pending && mbar_try_wait(&S.empty[s % NS], ((s / NS) - 1) & 1)) {
+      if (pending && mbar_test_wait(&S.empty[s % NS], ((s / NS) - 1) & 1)) {
         issue();
         pending = false;
       }
@@ -850,23 +850,23 @@ template <int BF16>
 __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) {
   fence_acq_rel_gpu();
   const int G = P.G, V = P.V, np = P.g.np_r, re = P.g.re;
+  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np_r4;
+  constexpr int kScrFloats = 1024;  // 4 KB
+  const bool staged = np <= kScrFloats;
+  // the mass copies and the stop-record load are in flight together
+  if (staged)
+    for (int k = lane * 4; k < np; k += 128) cp_async16(scr + k, rm + k);
   StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
   const float us = P.u_s[b];
   int32_t* tok = P.tok_out + (size_t)b * (G + 1);
-  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np_r4;
   const int n = st.n;
   int y = -1;
   ff T{0.f, 0.f};
-  constexpr int kScrFloats = 1024;  // 4 KB
+  cp_async_wait_all();
+  __syncwarp();
   if (st.mode != 2) {
     const unsigned char* trow = target_row(P, b, n);
     const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, n) : nullptr;
-    const bool staged = np <= kScrFloats;
-    if (staged) {
-      for (int k = lane * 4; k < np; k += 128) cp_async16(scr + k, rm + k);
-      cp_async_wait_all();
-    }
-    __syncwarp();
     const float* mv = staged ? scr : rm;
     const int per = (np + 31) / 32;
     const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
