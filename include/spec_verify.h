@@ -66,7 +66,9 @@ typedef enum sv_status {
   SV_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no GPU) */
   SV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
   SV_ERR_DEVICE_INPUT = 4, /* spec_verify_check: some row had invalid inputs   */
-  SV_ERR_TIMEOUT = 5       /* spec_verify_check: a bounded device wait ran out */
+  SV_ERR_TIMEOUT = 5,      /* spec_verify_check: a bounded device wait ran out */
+  SV_ERR_SCRATCH_LIMIT = 6 /* spec_verify_dense_static: sizes need more scratch
+                              than SV_STATIC_SCRATCH_BYTES; nothing launched  */
 } sv_status;
 
 typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -179,6 +181,47 @@ int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /* Static string for a status code. */
 const char* spec_verify_status_string(int status);
+
+/*
+ * spec_verify_dense_static -- spec_verify_dense for callers that cannot
+ * allocate device memory.  (Library plumbing: the paper has no counterpart.)
+ *
+ * Who needs it: code that must not call cudaMalloc or any other allocator
+ * where it verifies -- inside host callbacks or allocator hooks, plug-ins
+ * whose host runtime owns every allocation, loops that may not touch the
+ * allocator after start-up.  Such callers own their inputs and outputs but
+ * cannot provide the workspace, so this call takes its scratch from a fixed
+ * device array inside the library and allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *
+ * Arguments, layouts, outputs and results: exactly those of spec_verify_dense
+ * without the workspace; the same kernels run.
+ *
+ * The scratch: a file-scope device array of SV_STATIC_SCRATCH_BYTES (4 MiB),
+ * which every GPU that loads the library holds until the process exits.  A
+ * call needs spec_verify_workspace_size(B, gamma, V) bytes of it (for example
+ * 0.33 MiB at B = 64, gamma = 7, V = 128256; 2.75 MiB at B = 256, gamma = 15,
+ * V = 151936); larger sizes return SV_ERR_SCRATCH_LIMIT and launch nothing.
+ *   - Set-up: the first call on each device looks up the array's device
+ *     address (cudaGetSymbolAddress, with that device current) and keeps it.
+ *     That look-up may load the library's device code, so make the first
+ *     call on each device before any stream capture.
+ *   - Every call shares the array.  A call clears the part it uses (and sets
+ *     n_accepted to -1) on `stream` before its kernels run, so state left by
+ *     an earlier call never leaks in; calls whose work may overlap on the GPU
+ *     (other streams, other host threads) race on the array and must be
+ *     ordered by the caller.
+ *   - Errors: host-side argument errors as spec_verify_dense (nothing
+ *     launched).  There is no status word to query: rows with invalid inputs,
+ *     and rows a call left unfinished because a bounded wait ran out, carry
+ *     n_accepted = -1.
+ */
+#define SV_STATIC_SCRATCH_BYTES (4u << 20)
+int spec_verify_dense_static(const void* target_logits, const void* draft_logits, sv_dtype dtype,
+                             const int32_t* draft_ids, const float* u_accept,
+                             const float* u_sample, int B, int gamma, int V,
+                             int32_t* n_accepted, int32_t* out_tokens, float* residual_out,
+                             float* accept_prob_out, sv_stream_t stream);
 
 #ifdef __cplusplus
 }

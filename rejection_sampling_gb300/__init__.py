@@ -8,6 +8,8 @@ hand-written CUDA kernels for sm_103a in libspec_verify.so:
                         (small vocabularies: one warp per row)
   spec_verify_sparse    Uno-style sorted top-k (id, prob) support lists
   spec_verify_anyorder  masked-diffusion any-order window, small vocabulary
+  spec_verify_dense_static  spec_verify_dense on a static scratch array, for
+                        callers that cannot allocate device memory
 
 The Python functions below have the same names as the C entry points and only
 marshal torch tensors; the library is loaded lazily on first use and every
@@ -15,10 +17,11 @@ call fails loudly if it is missing.  ``workloads`` generates the seeded
 synthetic inputs.
 """
 from ._binding import (  # noqa: F401
-    EXPORTED, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_TIMEOUT,
-    SV_ERR_UNSUPPORTED, SV_F32, SV_OK, SpecVerifyError, VerifyResult, abi_version, check,
+    EXPORTED, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_SCRATCH_LIMIT,
+    SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_F32, SV_OK, SV_STATIC_SCRATCH_BYTES, SpecVerifyError,
+    VerifyResult, abi_version, check,
     debug_dense_ticket, get_workspace, library_path, load, prepare_anyorder, prepare_dense,
     prepare_sparse, PreparedCall, spec_verify_anyorder, spec_verify_dense,
-    spec_verify_sparse, status_string, workspace_size,
+    spec_verify_dense_static, spec_verify_sparse, status_string, workspace_size,
 )
 from ._build import build  # noqa: F401

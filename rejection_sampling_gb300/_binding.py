@@ -17,14 +17,16 @@ import torch
 
 from . import _build
 
-SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT = range(6)
+(SV_OK, SV_ERR_INVALID_ARG, SV_ERR_UNSUPPORTED, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_TIMEOUT,
+ SV_ERR_SCRATCH_LIMIT) = range(7)
+SV_STATIC_SCRATCH_BYTES = 4 << 20
 SV_F32, SV_BF16 = 0, 1
 
 # Every function declared in include/spec_verify.h and include/spec_verify_debug.h.
 EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
-    "spec_verify_status_string", "sv_debug_dense_ticket",
+    "spec_verify_status_string", "spec_verify_dense_static", "sv_debug_dense_ticket",
 )
 
 
@@ -72,6 +74,8 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_check.argtypes = [P, Z, P]
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.spec_verify_status_string.argtypes = [I]
+        lib.spec_verify_dense_static.restype = I
+        lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         lib.sv_debug_dense_ticket.restype = I
         lib.sv_debug_dense_ticket.argtypes = [ctypes.c_longlong, ctypes.c_longlong, I, I, I,
                                               ctypes.POINTER(ctypes.c_longlong)]
@@ -196,6 +200,42 @@ def spec_verify_dense(target_logits: torch.Tensor, draft_logits: torch.Tensor,
             _ptr(out.residual), _ptr(out.accept_prob), ws.data_ptr(), ws.numel(), sp)
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_dense")
+    return out
+
+
+def spec_verify_dense_static(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                             draft_ids: torch.Tensor, u_accept: torch.Tensor,
+                             u_sample: torch.Tensor, out: VerifyResult,
+                             stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """spec_verify_dense on the library's static scratch, for callers that
+    cannot allocate: the outputs are the caller's (``out``), nothing is
+    allocated here or in the library."""
+    lib = load()
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_dense_static needs CUDA tensors")
+    dt = _logit_dtype(target_logits)
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    _req(target_logits, "target_logits", target_logits.dtype, (B, G + 1, V), dev)
+    _req(draft_logits, "draft_logits", target_logits.dtype, (B, G, V), dev)
+    _req(draft_ids, "draft_ids", torch.int32, (B, G), dev)
+    _req(u_accept, "u_accept", torch.float32, (B, G), dev)
+    _req(u_sample, "u_sample", torch.float32, (B,), dev)
+    _req(out.n_accepted, "n_accepted", torch.int32, (B,), dev)
+    _req(out.out_tokens, "out_tokens", torch.int32, (B, G + 1), dev)
+    if out.residual is not None:
+        _req(out.residual, "residual", torch.float32, (B, V), dev)
+    if out.accept_prob is not None:
+        _req(out.accept_prob, "accept_prob", torch.float32, (B, G), dev)
+    sp = _stream_ptr(stream, dev)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_dense_static(
+            _ptr(target_logits), _ptr(draft_logits) if G > 0 else None, dt, _ptr(draft_ids),
+            _ptr(u_accept), _ptr(u_sample), B, G, V, _ptr(out.n_accepted), _ptr(out.out_tokens),
+            _ptr(out.residual), _ptr(out.accept_prob), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_dense_static")
     return out
 
 

@@ -256,6 +256,7 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_CUDA: return "CUDA error";
     case SV_ERR_DEVICE_INPUT: return "invalid input rows (n_accepted = -1)";
     case SV_ERR_TIMEOUT: return "bounded device wait expired; re-initialise the workspace";
+    case SV_ERR_SCRATCH_LIMIT: return "sizes need more than the library's static scratch";
     default: return "unknown status";
   }
 }
