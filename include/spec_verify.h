@@ -42,9 +42,9 @@
  *     contains NaN or +inf or is entirely -inf) do not stop the call: the
  *     offending row gets n_accepted = -1 and out_tokens = -1, and a bit is
  *     set in the workspace status word that spec_verify_check() reports.
- *   - No kernel ever waits without a bound.  If a bounded wait runs out, the
- *     call leaves its outputs undefined, sets the timeout bit, and the
- *     workspace must be re-initialised with spec_verify_workspace_init().
+ *   - No kernel waits on another thread block: work is handed on by
+ *     per-row arrival counters.  (SV_ERR_TIMEOUT is kept for ABI stability;
+ *     this version never reports it.)
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -66,7 +66,7 @@ typedef enum sv_status {
   SV_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no GPU) */
   SV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
   SV_ERR_DEVICE_INPUT = 4, /* spec_verify_check: some row had invalid inputs   */
-  SV_ERR_TIMEOUT = 5,      /* spec_verify_check: a bounded device wait ran out */
+  SV_ERR_TIMEOUT = 5,      /* reserved: a bounded device wait ran out        */
   SV_ERR_SCRATCH_LIMIT = 6 /* spec_verify_dense_static: sizes need more scratch
                               than SV_STATIC_SCRATCH_BYTES; nothing launched  */
 } sv_status;
@@ -115,8 +115,10 @@ sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream
  *                 every j (all positions are scored, as in the parallel pass)
  * Softmax, gather, ratio test, first-reject scan and the inverse-CDF draw run
  * in fp32, with partial sums combined and prefixed in float-float (pairs of
- * fp32 carrying ~48 significant bits); bf16 inputs are widened
- * exactly.  One fused persistent kernel reads each logit once from HBM.
+ * fp32 carrying ~48 significant bits); bf16 inputs are widened exactly.
+ * Large vocabularies take two kernels: the first reads every logit once
+ * (statistics, gather, accept tests, first rejection), the second reads the
+ * two rows of each row's stop position again (residual masses and the draw).
  */
 int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dtype dtype,
                       const int32_t* draft_ids, const float* u_accept, const float* u_sample,
@@ -174,8 +176,7 @@ int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv
  * spec_verify_check -- synchronise `stream`, read and clear the workspace
  * status word.  Returns SV_OK, SV_ERR_DEVICE_INPUT (some row of an earlier
  * call had invalid inputs; those rows carry n_accepted = -1),
- * SV_ERR_TIMEOUT (a bounded wait ran out; re-initialise the workspace) or
- * SV_ERR_CUDA.
+ * or SV_ERR_CUDA.
  */
 int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream);
 

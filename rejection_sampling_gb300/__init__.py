@@ -20,7 +20,7 @@ from ._binding import (  # noqa: F401
     EXPORTED, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_SCRATCH_LIMIT,
     SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_F32, SV_OK, SV_STATIC_SCRATCH_BYTES, SpecVerifyError,
     VerifyResult, abi_version, check,
-    debug_dense_ticket, get_workspace, library_path, load, prepare_anyorder, prepare_dense,
+    get_workspace, library_path, load, prepare_anyorder, prepare_dense,
     prepare_sparse, PreparedCall, spec_verify_anyorder, spec_verify_dense,
     spec_verify_dense_static, spec_verify_sparse, status_string, workspace_size,
 )

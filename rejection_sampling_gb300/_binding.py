@@ -22,11 +22,11 @@ from . import _build
 SV_STATIC_SCRATCH_BYTES = 4 << 20
 SV_F32, SV_BF16 = 0, 1
 
-# Every function declared in include/spec_verify.h and include/spec_verify_debug.h.
+# Every function declared in include/spec_verify.h.
 EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
-    "spec_verify_status_string", "spec_verify_dense_static", "sv_debug_dense_ticket",
+    "spec_verify_status_string", "spec_verify_dense_static",
 )
 
 
@@ -76,9 +76,6 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_status_string.argtypes = [I]
         lib.spec_verify_dense_static.restype = I
         lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
-        lib.sv_debug_dense_ticket.restype = I
-        lib.sv_debug_dense_ticket.argtypes = [ctypes.c_longlong, ctypes.c_longlong, I, I, I,
-                                              ctypes.POINTER(ctypes.c_longlong)]
         _lib = lib
         return lib
 
@@ -319,15 +316,6 @@ def spec_verify_anyorder(target_logits: torch.Tensor, draft_logits: torch.Tensor
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_anyorder")
     return res
-
-
-def debug_dense_ticket(t: int, B: int, gamma: int, V: int, es: int):
-    """(row, position, unit) of statistics ticket t of the dense kernel."""
-    out = (ctypes.c_longlong * 3)()
-    rc = load().sv_debug_dense_ticket(int(t), int(B), int(gamma), int(V), int(es), out)
-    if rc != SV_OK:
-        raise SpecVerifyError(rc, "sv_debug_dense_ticket")
-    return int(out[0]), int(out[1]), int(out[2])
 
 
 class PreparedCall:

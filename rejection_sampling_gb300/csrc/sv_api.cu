@@ -9,19 +9,6 @@
 
 namespace {
 
-constexpr long long kWaitBoundCycles = 4000000000LL;  // ~2 s at GB300 clocks
-
-int sm_count_for_current_device() {
-  static int cached[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev >= 0 && dev < 64) cached[dev] = n;
-  return n;
-}
-
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // The small warp-per-row kernel handles R <= 32 rows per warp if the staged
@@ -106,8 +93,8 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
   const sv::DenseGeom g = sv::dense_geom(V, es);
   const sv::DenseLayout L = sv::dense_layout(B, gamma, g);
   if (ws_bytes < L.total) return SV_ERR_INVALID_ARG;
-  const int sms = sm_count_for_current_device();
-  if (sms <= 0) return SV_ERR_CUDA;
+  // one CTA per (row, position, chunk) and per (row, chunk): 31-bit grids
+  if ((long long)B * (gamma + 1) * g.nc >= (1ll << 31) - 1) return SV_ERR_INVALID_ARG;
   sv::DenseParams p;
   memset(&p, 0, sizeof p);
   p.lt = static_cast<const unsigned char*>(target_logits);
@@ -127,21 +114,10 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
   p.bf16 = (dtype == SV_BF16);
   p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(target_logits, 16) &&
               (!draft_logits || aligned_to(draft_logits, 16));
-  p.tickets = (long long)(gamma + 1) * g.nc_s * (long long)B;
-  if ((long long)g.nc_r * B >= (1ll << 31) - 65536) return SV_ERR_INVALID_ARG;
-  p.resid_units = (unsigned)((long long)g.nc_r * B);
-  p.small_tickets = (p.tickets + 4 * 65536 < (1ll << 31)) ? 1 : 0;
-  long long grid = (long long)sms * sv::dense_ctas_per_sm();
-  if (grid > p.tickets) grid = p.tickets;
-  p.wait_bound = kWaitBoundCycles;
   p.keep_stop = residual_out != nullptr;
-  p.tk = sv::make_ticket_consts(gamma, g.nc_s);
-  cudaError_t e = sv::launch_dense(p, (int)grid, s);
-  if (e != cudaSuccess) return SV_ERR_CUDA;
-  if (residual_out) {
-    e = sv::launch_dense_resid_out(p, residual_out, s);
-    if (e != cudaSuccess) return SV_ERR_CUDA;
-  }
+  if (sv::launch_dense(p, s) != cudaSuccess) return SV_ERR_CUDA;
+  if (residual_out && sv::launch_dense_resid_out(p, residual_out, s) != cudaSuccess)
+    return SV_ERR_CUDA;
   return SV_OK;
 }
 
@@ -238,9 +214,8 @@ int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream) {
     return SV_ERR_CUDA;
   if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
   if (h.status) {
-    // clear status and abort (two adjacent words)
     sv::WsHeader* d = reinterpret_cast<sv::WsHeader*>(workspace);
-    if (cudaMemsetAsync(&d->status, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+    if (cudaMemsetAsync(&d->status, 0, sizeof(uint32_t), s) != cudaSuccess) return SV_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
   }
   if (h.status & sv::kStatusTimeout) return SV_ERR_TIMEOUT;
@@ -259,27 +234,6 @@ const char* spec_verify_status_string(int status) {
     case SV_ERR_SCRATCH_LIMIT: return "sizes need more than the library's static scratch";
     default: return "unknown status";
   }
-}
-
-// Host-side view of the dense kernel's statistics ticket order, for tests:
-// out3 = (row, position, unit) of ticket t.
-int sv_debug_dense_ticket(long long t, long long B, int gamma, int V, int es, long long* out3) {
-  if (!out3 || (es != 2 && es != 4) || B <= 0 || gamma < 0 || V <= 0) return SV_ERR_INVALID_ARG;
-  const sv::DenseGeom g = sv::dense_geom(V, es);
-  if (t < 0 || t >= (long long)(gamma + 1) * g.nc_s * B) return SV_ERR_INVALID_ARG;
-  int b = 0, j = 0, c = 0;
-  sv::dense_ticket(t, gamma, g.nc_s, &b, &j, &c);
-  out3[0] = b;
-  out3[1] = j;
-  out3[2] = c;
-  // the 32-bit decode the kernel uses must agree with plain division
-  if (t < (1ll << 31)) {
-    const sv::TicketConsts k = sv::make_ticket_consts(gamma, g.nc_s);
-    int b2 = 0, j2 = 0, c2 = 0;
-    sv::dense_ticket_fast((unsigned)t, k, &b2, &j2, &c2);
-    if (b2 != b || j2 != j || c2 != c) return SV_ERR_UNSUPPORTED;
-  }
-  return SV_OK;
 }
 
 }  // extern "C"

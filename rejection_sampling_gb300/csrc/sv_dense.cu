@@ -1,4 +1,6 @@
-// sv_dense.cu -- fused single-HBM-pass dense verification for large vocabularies.
+// sv_dense.cu -- dense verification for large vocabularies: two streaming
+// kernels, one HBM pass over every logit plus one pass over the two rows of
+// each row's stop position.
 //
 // Computes, for every row b (DFlash/DFlash2 guide, 4.4; Uno article, "What
 // 'lossless' actually has to mean"):
@@ -8,79 +10,38 @@
 //   token n = inverse CDF of max(p_n - q_n, 0) (n < gamma) or of p_gamma
 //   (bonus, DFlash/DFlash2 guide section 2) at u_sample[b].
 //
-// Design (one persistent kernel, one launch per call):
-//  * Statistics work is a stream of tickets in row order, taken with one
-//    atomicAdd each (prefetched one ahead).  A statistics unit is up to
-//    8 x 4 KB pieces of the target row (b, j) plus the same pieces of the
-//    draft row (b, j).  When a row's statistics are complete its finaliser
-//    publishes the row's residual units -- up to 8 pieces of 2 KB target +
-//    2 KB draft of the stop position (b, n) -- to a queue that producers
-//    drain before taking new tickets.
-//  * Each CTA = 1 producer warp + NW consumer warps + 1 finaliser warp around
-//    an NS-stage ring of 4 KB shared-memory stages.  The producer moves pieces with 1-D bulk
-//    copies (cp.async.bulk, TMA) completing on per-stage mbarriers; consumer
-//    warp w takes stages w, w + NW, ...  A consumer releases its stage as soon
-//    as the data is in registers, so slow bookkeeping never holds the ring.
-//  * A consumer warp reduces a 4 KB piece to (c, s): c = log2e * max, s =
-//    sum 2^(v*log2e - c) (MUFU ex2).  The last warp of a unit combines the
-//    unit's pieces and publishes one partial; the last unit of a row runs all
-//    of the row's accept tests (one lane per position), finds the first
-//    rejection n and publishes the stop constants.  These
-//    hand-offs are last-arriver atomics; the consumer that completes a row
-//    queues the row for its CTA's finaliser warp, so the latency of the
-//    row-level work never stalls the data pipeline.  No warp ever waits for
-//    another CTA
-//    while it holds statistics work.  A producer waits (bounded) for a queue
-//    entry only once every statistics ticket is taken; every such entry is
-//    published by a row whose statistics units are all held by running CTAs
-//    that never wait, so the wait always ends.
-//  * Residual units recompute r(y) = max(p(y) - q(y), 0) for the stop
-//    position only (the rows are still in L2: they were read a few rows of
-//    work earlier) and publish per-piece masses; the last one selects the
-//    piece and then the token by a float-float prefix over fp32 element values.
+// Design.
+//  * A logit row is cut into 2 KB pieces; a CTA of 16 warps takes 16
+//    consecutive pieces (a 32 KB chunk), one warp per piece.
+//  * dense_stats_kernel: one CTA per (row b, position j, chunk c), launched
+//    row by row.  Each warp loads its target piece and the same draft piece
+//    straight into registers (16-byte loads, all in flight together), reduces
+//    each to (c, S) -- c = log2e * max (max.bf16x2), S = sum 2^(v log2e - c)
+//    (ex2.approx) -- and the warp holding the draft token x_j picks up the two
+//    logits there.  Warp 0 combines the 16 pieces in float-float and writes
+//    the chunk's partial.  The CTA that completes a row (a per-row arrival
+//    counter) finalises it: combines every position's partials, forms the
+//    ratios, runs the accept tests, finds n and writes the stop record, the
+//    accept probabilities and every token but the one drawn at n.  Rows
+//    complete in launch order, so all but the last rows' finalisations
+//    overlap the stream of later rows.
+//  * dense_resid_kernel: one CTA per (row b, chunk c) recomputes
+//    r(y) = max(p_n(y) - q_n(y), 0) (or p_gamma) over its chunk of the stop
+//    position's two rows and writes one mass per piece.  The CTA completing
+//    the row draws the token: a float-float prefix over the piece masses picks
+//    the piece, then a prefix over the piece's fp32 values picks y.
+//  * No thread ever waits for another CTA: hand-offs are last-arriver
+//    counters, which the finishing CTA resets, and every array a call reads is
+//    written earlier in the same call.  The workspace is all zero again after
+//    every call.
 #include "sv_common.cuh"
 
 namespace sv {
 namespace {
 
-enum StageKind : int { kStatsT = 0, kStatsD = 1, kResid = 2, kResidSkip = 3, kEnd = 4 };
-
-struct StageMeta {
-  int kind, b, j, kp, ne, uslot, upieces, pidx, unit_c, npc, mode, pad;
-  float ct, cd, invSt, invSd;
-};
-
-struct UnitSlot {
-  unsigned int count;
-  unsigned int pad[3];
-  float c[2 * kUnitPieces];
-  float s[2 * kUnitPieces];
-};
-
-constexpr int kFinQ = 64;  // finaliser queue entries
-
-template <int NS, int NW>
-struct Smem {
-  // Stage s lives in slot s % NS and is consumed by warp s % NW.  With NS a
-  // multiple of NW the stage that last used a slot (s - NS) belongs to the
-  // same warp, which consumed it first; a warp can therefore never wait on a
-  // slot two phases ahead, where an mbarrier parity wait would alias.
-  static_assert(NS % NW == 0, "ring depth must be a multiple of the consumer warps");
-  static constexpr int NU = 2 * NS;  // unit slots
-  alignas(128) unsigned char ring[NS][kPieceBytes];
-  uint64_t full[NS];
-  uint64_t empty[NS];
-  uint64_t ufree[NU];
-  StageMeta meta[NS];
-  UnitSlot unit[NU];
-  // consumer -> finaliser hand-off: +(b+1) finalise row b, -(b+1) select its token
-  UnitPart fin_scratch[128];  // finaliser staging (4 KB)
-  int fin_item[kFinQ];
-  unsigned fin_seq[kFinQ];
-  unsigned fin_tail;
-  unsigned fin_head;
-  unsigned cons_done;
-};
+constexpr int kWarps = kChunkPieces;  // warps per CTA, one piece each
+constexpr int kThreads = 32 * kWarps;
+constexpr int kMaxG = 256;            // positions per row (gamma + 1 <= 256)
 
 // ---------------------------------------------------------------------------
 // workspace accessors
@@ -103,6 +64,13 @@ __device__ __forceinline__ T ldcg32(const T* p) {
   o[0] = a;
   o[1] = b;
   return out;
+}
+template <class T>
+__device__ __forceinline__ void zero32(T* p) {
+  static_assert(sizeof(T) == 32, "32-byte record");
+  int4* q = reinterpret_cast<int4*>(p);
+  q[0] = make_int4(0, 0, 0, 0);
+  q[1] = make_int4(0, 0, 0, 0);
 }
 
 __device__ __forceinline__ const unsigned char* target_row(const DenseParams& P, int b, int j) {
@@ -132,477 +100,89 @@ __device__ __forceinline__ float resid_val(float t, float d, float ct, float cd,
   return r > 0.f ? r : 0.f;
 }
 
-// ---------------------------------------------------------------------------
-// bounded waits (every spin has a limit; on expiry: timeout + abort flags and
-// the first expired site recorded in the header for diagnosis)
-// ---------------------------------------------------------------------------
-enum WaitSite : unsigned {
-  kSiteProdEmpty = 1, kSiteProdUnit = 2, kSiteEntry = 4, kSiteConsFull = 5, kSiteFinPush = 6,
-  kSiteFinIdle = 7
-};
-
-__device__ void record_timeout(const DenseParams& P, unsigned site, unsigned info) {
-  WsHeader* h = hdr_of(P);
-  if (atomicCAS(&h->timeout_site, 0u, site) == 0u) h->timeout_info = info;
-  atomicOr(&h->status, kStatusTimeout);
-  atomicExch(&h->abort, 1u);
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-__device__ bool wait_phase(uint64_t* bar, uint32_t parity, const DenseParams& P, unsigned site,
-                           unsigned info) {
-  if (mbar_try_wait(bar, parity)) return true;
-  WsHeader* h = hdr_of(P);
-  const long long t0 = clock64();
-  unsigned it = 0;
-  while (!mbar_try_wait(bar, parity)) {
-    if ((++it & 63u) == 0) {
-      if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return false;
-      if (clock64() - t0 > P.wait_bound) {
-        record_timeout(P, site, info);
-        return false;
-      }
-    }
-  }
-  return true;
-}
-
-// ---------------------------------------------------------------------------
-// ticket -> work unit
-// ---------------------------------------------------------------------------
-struct Unit {
-  int b, j, c;
-};
-
-__device__ __forceinline__ Unit decode_ticket(long long t, const DenseParams& P) {
-  Unit u;
-  if (P.small_tickets)
-    dense_ticket_fast((unsigned)t, P.tk, &u.b, &u.j, &u.c);
-  else
-    dense_ticket(t, P.G, P.g.nc_s, &u.b, &u.j, &u.c);
-  return u;
-}
-
-// residual queue entry: (row + 1) << 32 | unit, 0 while unpublished
-__device__ __forceinline__ unsigned long long* rq_of(const DenseParams& P) {
-  return ws_at<unsigned long long>(P, P.L.rq);
-}
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u64(unsigned long long* p, unsigned long long v) {
-  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+// streaming 16-byte load: no L1 allocation (every byte is read once here)
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
   return v;
 }
 
-// producer lane 0: wait until residual queue entry i is published (bounded)
-__device__ unsigned long long wait_entry(const DenseParams& P, unsigned i) {
-  const unsigned long long* e = rq_of(P) + i;
-  unsigned long long v = ld_acquire_u64(e);
-  if (v) return v;
-  WsHeader* h = hdr_of(P);
-  const long long t0 = clock64();
-  while (!(v = ld_acquire_u64(e))) {
-    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) return 0;
-    if (clock64() - t0 > P.wait_bound) {
-      record_timeout(P, kSiteEntry, i);
-      return 0;
-    }
-    nanosleep_ns(64);
-  }
-  return v;
-}
+constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // two bf16 -inf
+constexpr uint32_t kNegInfF = 0xFF800000u;  // fp32 -inf
 
 // ---------------------------------------------------------------------------
-// producer
+// one 2 KB piece per warp: lane holds 16-byte vectors lane + 32 i, i < 4
+// (8 bf16 or 4 fp32 elements each); elements past `ne` read as -inf
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void copy_plain(unsigned char* dst, const unsigned char* src, int bytes,
-                                           int es, int lane) {
-  if (es == 2) {
-    const uint16_t* s = reinterpret_cast<const uint16_t*>(src);
-    uint16_t* d = reinterpret_cast<uint16_t*>(dst);
-    for (int i = lane; i < bytes / 2; i += 32) d[i] = s[i];
-  } else {
-    const uint32_t* s = reinterpret_cast<const uint32_t*>(src);
-    uint32_t* d = reinterpret_cast<uint32_t*>(dst);
-    for (int i = lane; i < bytes / 4; i += 32) d[i] = s[i];
-  }
-}
-
-// fill stage `slot` with up to two row slices; completes full[slot]
-template <int NS, int NW>
-__device__ __forceinline__ void issue_stage(const DenseParams& P, Smem<NS, NW>& S, int slot,
-                                            const unsigned char* src0, int bytes0,
-                                            const unsigned char* src1, int bytes1, int lane) {
-  if (P.aligned) {
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(bytes0 + bytes1));
-      if (bytes0) bulk_g2s(S.ring[slot], src0, (uint32_t)bytes0, &S.full[slot]);
-      if (bytes1) bulk_g2s(S.ring[slot] + kResidRowBytes, src1, (uint32_t)bytes1, &S.full[slot]);
-    }
-  } else {
-    if (bytes0) copy_plain(S.ring[slot], src0, bytes0, P.g.es, lane);
-    if (bytes1) copy_plain(S.ring[slot] + kResidRowBytes, src1, bytes1, P.g.es, lane);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&S.full[slot]);
-  }
-}
-
-template <int NS, int NW>
-__device__ void producer(const DenseParams& P, Smem<NS, NW>& S, int lane) {
-  constexpr int NU = Smem<NS, NW>::NU;
-  WsHeader* h = hdr_of(P);
-  const int G = P.G, V = P.V, es = P.g.es;
-  uint32_t seq = 0, useq = 0;
-  bool ok = true;
-
-  auto acquire = [&](uint32_t s) -> bool {
-    if (s < (uint32_t)NS) return true;
-    return wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P, kSiteProdEmpty, s);
-  };
-  auto acquire_unit = [&](uint32_t u) -> bool {
-    if (u < (uint32_t)NU) return true;
-    return wait_phase(&S.ufree[u % NU], ((u / NU) - 1) & 1, P, kSiteProdUnit, u);
-  };
-  // Stage i of a unit is issued by lane i: its own ring-slot wait, metadata,
-  // expect-tx and bulk copy.  A lane issues as soon as its slot is free, so the
-  // ring refills stage by stage rather than a whole unit at a time.  (Rows
-  // that are not 16-byte aligned take the warp-wide plain-copy path.)
-  auto lane_acquire = [&](bool mine, uint32_t s) -> bool {
-    bool ok_l = true;
-    if (mine && s >= (uint32_t)NS)
-      ok_l = wait_phase(&S.empty[s % NS], ((s / NS) - 1) & 1, P, kSiteProdEmpty, s);
-    return __all_sync(0xffffffffu, ok_l);
-  };
-  // run issue(lane) on every lane with `mine` as soon as its stage's slot is free
-  auto lane_issue = [&](bool mine, uint32_t s, auto&& issue) -> bool {
-    bool pending = mine;
-    if (pending && s < (uint32_t)NS) {
-      issue();
-      pending = false;
-    }
-    const long long t0 = clock64();
-    unsigned it = 0;
-    while (__any_sync(0xffffffffu, pending)) {
-      if (pending && mbar_test_wait(&S.empty[s % NS], ((s / NS) - 1) & 1)) {
-        issue();
-        pending = false;
-      }
-      if ((++it & 63u) == 0) {
-        bool stop = *reinterpret_cast<volatile uint32_t*>(&h->abort) != 0;
-        if (!stop && clock64() - t0 > P.wait_bound) {
-          if (pending) record_timeout(P, kSiteProdEmpty, s);
-          stop = true;
-        }
-        if (__any_sync(0xffffffffu, stop)) return false;
-      }
-    }
-    return true;
-  };
-
-  auto issue_stats = [&](const Unit& u) -> bool {
-    if (!acquire_unit(useq)) return false;
-    const int uslot = useq % NU;
-    ++useq;
-    const int npc = min(kUnitPieces, P.g.np_s - u.c * kUnitPieces);
-    const int up = (u.j < G) ? 2 * npc : npc;
-    if (P.aligned) {
-      const int pi = lane;
-      const bool mine = pi < up;
-      const uint32_t sq = seq + (uint32_t)pi;
-      const bool ok_i = lane_issue(mine, sq, [&]() {
-        const int isd = pi >= npc;
-        const int kp = u.c * kUnitPieces + (isd ? pi - npc : pi);
-        const int ne = min(P.g.pe, V - kp * P.g.pe);
-        const unsigned char* row = isd ? draft_row(P, u.b, u.j) : target_row(P, u.b, u.j);
-        const int slot = sq % NS;
-        StageMeta& m = S.meta[slot];
-        m.kind = isd ? kStatsD : kStatsT;
-        m.b = u.b;
-        m.j = u.j;
-        m.kp = kp;
-        m.ne = ne;
-        m.uslot = uslot;
-        m.upieces = up;
-        m.pidx = pi;
-        m.unit_c = u.c;
-        m.npc = npc;
-        mbar_arrive_expect_tx(&S.full[slot], (uint32_t)(ne * es));
-        bulk_g2s(S.ring[slot], row + (size_t)kp * kPieceBytes, (uint32_t)(ne * es), &S.full[slot]);
-      });
-      seq += (uint32_t)up;
-      return ok_i;
-    }
-    for (int pi = 0; pi < up; ++pi) {
-      const int isd = pi >= npc;
-      const int kp = u.c * kUnitPieces + (isd ? pi - npc : pi);
-      const int ne = min(P.g.pe, V - kp * P.g.pe);
-      const unsigned char* row = isd ? draft_row(P, u.b, u.j) : target_row(P, u.b, u.j);
-      if (!acquire(seq)) return false;
-      const int slot = seq % NS;
-      if (lane == 0) {
-        StageMeta& m = S.meta[slot];
-        m.kind = isd ? kStatsD : kStatsT;
-        m.b = u.b;
-        m.j = u.j;
-        m.kp = kp;
-        m.ne = ne;
-        m.uslot = uslot;
-        m.upieces = up;
-        m.pidx = pi;
-        m.unit_c = u.c;
-        m.npc = npc;
-      }
-      issue_stage(P, S, slot, row + (size_t)kp * kPieceBytes, ne * es, nullptr, 0, lane);
-      ++seq;
-    }
-    return true;
-  };
-
-  // residual unit (b, c) of a row whose stop constants are published
-  auto issue_resid = [&](int b, int c) -> bool {
-    if (!acquire_unit(useq)) return false;
-    const int uslot = useq % NU;
-    ++useq;
-    const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
-    const int npc = min(kUnitPieces, P.g.np_r - c * kUnitPieces);
-    const unsigned char* trow = target_row(P, b, st.n);
-    const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
-    auto fill_meta = [&](StageMeta& m, int kp, int ne, int pi) {
-      m.kind = (st.mode == 2) ? kResidSkip : kResid;
-      m.b = b;
-      m.j = st.n;
-      m.kp = kp;
-      m.ne = ne;
-      m.uslot = uslot;
-      m.upieces = npc;
-      m.pidx = pi;
-      m.unit_c = c;
-      m.npc = npc;
-      m.mode = st.mode;
-      m.ct = st.ct;
-      m.cd = st.cd;
-      m.invSt = st.invSt;
-      m.invSd = st.invSd;
-    };
-    if (P.aligned || st.mode == 2) {
-      const int pi = lane;
-      const bool mine = pi < npc;
-      const uint32_t sq = seq + (uint32_t)pi;
-      const bool ok_i = lane_issue(mine, sq, [&]() {
-        const int kp = c * kUnitPieces + pi;
-        const int ne = min(P.g.re, V - kp * P.g.re);
-        const int slot = sq % NS;
-        fill_meta(S.meta[slot], kp, ne, pi);
-        if (st.mode == 2) {
-          mbar_arrive(&S.full[slot]);
-        } else {
-          const size_t off = (size_t)kp * kResidRowBytes;
-          const uint32_t bytes = (uint32_t)(ne * es);
-          mbar_arrive_expect_tx(&S.full[slot], drow ? 2 * bytes : bytes);
-          bulk_g2s(S.ring[slot], trow + off, bytes, &S.full[slot]);
-          if (drow) bulk_g2s(S.ring[slot] + kResidRowBytes, drow + off, bytes, &S.full[slot]);
-        }
-      });
-      seq += (uint32_t)npc;
-      return ok_i;
-    }
-    for (int pi = 0; pi < npc; ++pi) {
-      const int kp = c * kUnitPieces + pi;
-      const int ne = min(P.g.re, V - kp * P.g.re);
-      if (!acquire(seq)) return false;
-      const int slot = seq % NS;
-      if (lane == 0) fill_meta(S.meta[slot], kp, ne, pi);
-      const size_t off = (size_t)kp * kResidRowBytes;
-      issue_stage(P, S, slot, trow + off, ne * es, drow ? drow + off : nullptr,
-                  drow ? ne * es : 0, lane);
-      ++seq;
-    }
-    return true;
-  };
-
-  // Work loop.  Ready residual work (published by row finalisers) is taken
-  // first -- its rows were just read and are still in L2 -- otherwise the next
-  // statistics ticket.  Every global round trip of the loop (the next ticket,
-  // the queue counters, a queue claim, the value of a claimed entry) is issued
-  // by lane 0 one iteration ahead and consumed in the next, so while
-  // statistics work remains the producer never stalls on a round trip.  A
-  // claimed entry that is not yet published is waited for only when no
-  // statistics ticket is left.
-  enum : int { kActStats = 0, kActResid = 1, kActWait = 2, kActClaim = 3, kActDone = 4 };
-  constexpr uint32_t kNone = 0xffffffffu;
-  WsHeader* hq = h;
-  unsigned long long next = 0;     // prefetched statistics ticket
-  uint32_t v_head = 0, v_res = 0;  // queue counters seen one iteration ago
-  uint32_t claim = kNone;          // queue claim issued last iteration
-  unsigned long long ev = 0;       // entry[held] as loaded last iteration
-  long long held = -1;             // claimed queue entry not yet issued
-  if (lane == 0) {
-    next = atomicAdd(&h->ticket, 1ull);
-    v_head = ld_relaxed_u32(&hq->rq_head);
-    v_res = ld_relaxed_u32(&hq->rq_reserve);
-  }
-  while (ok) {
-    if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
-      ok = false;
-      break;
-    }
-    int act = kActStats;
-    if (lane == 0) {
-      const bool stats_left = (long long)next < P.tickets;
-      if (claim != kNone) {  // resolve last iteration's claim
-        if (claim < P.resid_units) {
-          held = claim;
-          ev = 0;  // its value is loaded below, for the next iteration
-        } else if (!stats_left) {
-          act = kActDone;  // every residual unit is claimed
-        }
-        claim = kNone;
-      }
-      if (act != kActDone) {
-        if (held >= 0 && ev != 0)
-          act = kActResid;
-        else if (held >= 0 && !stats_left)
-          act = kActWait;
-        else if (stats_left)
-          act = kActStats;
-        else
-          act = kActClaim;
-      }
-    }
-    act = __shfl_sync(0xffffffffu, act, 0);
-    if (act == kActDone) break;
-    if (act == kActResid || act == kActWait) {
-      unsigned long long e = 0;
-      if (lane == 0) {
-        // acquire: the row's stop record was written before the entry
-        e = (act == kActWait) ? wait_entry(P, (unsigned)held) : ld_acquire_u64(rq_of(P) + held);
-        if (e) rq_of(P)[held] = 0ull;  // self-reset for the next call
-        held = -1;
-      }
-      e = __shfl_sync(0xffffffffu, e, 0);
-      __syncwarp();
-      if (!e) {  // the bounded wait ran out
-        ok = false;
-        break;
-      }
-      ok = issue_resid((int)(e >> 32) - 1, (int)(e & 0xffffffffu));
-    } else if (act == kActStats) {
-      const unsigned long long t = __shfl_sync(0xffffffffu, next, 0);
-      if (lane == 0) next = atomicAdd(&h->ticket, 1ull);  // next ticket, used next iteration
-      ok = issue_stats(decode_ticket((long long)t, P));
-    } else {  // kActClaim: no statistics left; the claim resolves next iteration
-      if (lane == 0) claim = atomicAdd(&hq->rq_head, 1u);
-    }
-    // round trips for the next iteration
-    if (lane == 0) {
-      if (held >= 0) {
-        ev = ld_relaxed_u64(rq_of(P) + held);
-      } else if (claim == kNone && v_head < v_res && (long long)next < P.tickets) {
-        claim = atomicAdd(&hq->rq_head, 1u);  // published work is waiting: claim one
-      }
-      v_head = ld_relaxed_u32(&hq->rq_head);
-      v_res = ld_relaxed_u32(&hq->rq_reserve);
-    }
-  }
-  // one end marker per consumer warp (lane w marks the stage consumer w takes next)
-  static_assert(NW <= 32, "one lane per consumer warp");
-  if (ok) {
-    const bool mine = lane < NW;
-    const uint32_t sq = seq + (uint32_t)lane;
-    ok = lane_acquire(mine, sq);
-    if (ok && mine) {
-      const int slot = sq % NS;
-      S.meta[slot].kind = kEnd;
-      mbar_arrive(&S.full[slot]);
-    }
-    seq += NW;
-  }
-  // never leave the CTA with bulk copies in flight
-  if (lane == 0) {
-    const uint32_t first = seq > (uint32_t)NS ? seq - NS : 0u;
-    for (uint32_t s = first; s < seq; ++s) {
-      const int slot = s % NS;
-      if (!mbar_try_wait(&S.full[slot], (s / NS) & 1)) {
-        const long long t0 = clock64();
-        while (!mbar_try_wait(&S.full[slot], (s / NS) & 1) && clock64() - t0 < P.wait_bound) {
-        }
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// consumer: statistics of one 4 KB piece.  Releases the stage (`release`)
-// as soon as every loaded register has been consumed.
-// ---------------------------------------------------------------------------
-template <class Release>
-__device__ __forceinline__ void stats_piece(const unsigned char* slot, int ne, int bf16, int lane,
-                                            float& c_out, float& s_out, Release release) {
-  const uint4* v = reinterpret_cast<const uint4*>(slot);
-  constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // two bf16 -inf
-  uint4 r[8];
-  const int epv = bf16 ? 8 : 4;  // elements per 16-byte vector
-  const int nv = (ne + epv - 1) / epv;
+__device__ __forceinline__ void load_piece(const unsigned char* base, int ne, int bf16,
+                                           int aligned, int lane, uint4 (&r)[4]) {
+  const int epv = bf16 ? 8 : 4;
+  const uint32_t ninf = bf16 ? kNegInf2 : kNegInfF;
+  if (aligned) {  // row bytes are a multiple of 16: every vector is whole
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      r[i] = (vi * epv < ne) ? ld_stream(base + 16 * (size_t)vi) : make_uint4(ninf, ninf, ninf, ninf);
+    }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
     const int vi = lane + 32 * i;
-    if (vi < nv) {
-      r[i] = v[vi];
-      const int rem = ne - vi * epv;  // valid elements in this vector
-      if (rem < epv) {                // ragged tail: mask to -inf
-        uint32_t* w = reinterpret_cast<uint32_t*>(&r[i]);
-        if (bf16) {
+    uint32_t w[4];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (e >= rem) {
-              uint32_t& ww = w[e >> 1];
-              ww = (e & 1) ? ((ww & 0x0000FFFFu) | 0xFF800000u) : ((ww & 0xFFFF0000u) | 0xFF80u);
-            }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (e >= rem) w[e] = 0xFF800000u;
-        }
+    for (int q = 0; q < 4; ++q) {
+      if (bf16) {
+        const int e0 = vi * 8 + 2 * q;
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(base);
+        const uint32_t lo = (e0 < ne) ? h[e0] : 0xFF80u;
+        const uint32_t hi = (e0 + 1 < ne) ? h[e0 + 1] : 0xFF80u;
+        w[q] = lo | (hi << 16);
+      } else {
+        const int e = vi * 4 + q;
+        w[q] = (e < ne) ? reinterpret_cast<const uint32_t*>(base)[e] : kNegInfF;
       }
-    } else {
-      r[i] = bf16 ? make_uint4(kNegInf2, kNegInf2, kNegInf2, kNegInf2)
-                  : make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u);
     }
+    r[i] = make_uint4(w[0], w[1], w[2], w[3]);
   }
+}
+
+// (c, S) of a piece: c = log2e * max, S = sum 2^(v log2e - c); an all -inf
+// piece gives c = -inf, S = 0 (its exponentials use c = 0, so a NaN still
+// poisons S)
+__device__ __forceinline__ void piece_stats(const uint4 (&r)[4], int bf16, float& c_out,
+                                            float& s_out) {
   float m;
   if (bf16) {
     uint32_t mx = kNegInf2;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
       mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(r[i].x, r[i].y), bf16x2_max(r[i].z, r[i].w)));
     m = fmaxf(bf16_lo(mx), bf16_hi(mx));
   } else {
     m = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < 4; ++i)
       m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(r[i].x), __uint_as_float(r[i].y)),
                          fmaxf(__uint_as_float(r[i].z), __uint_as_float(r[i].w))));
   }
-  // every loaded register has been read by the max: hand the stage back
-  release();
   m = warp_max(m);
-  // c = log2e * max; an all -inf piece keeps c = 0 so NaN inputs still poison s
   const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (bf16) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -c));
       a1 += ex2(fmaf(bf16_hi(r[i].x), kLog2e, -c));
       a2 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -c));
@@ -614,7 +194,7 @@ __device__ __forceinline__ void stats_piece(const unsigned char* slot, int ne, i
     }
   } else {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < 4; ++i) {
       a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -c));
       a1 += ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -c));
       a2 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -c));
@@ -625,61 +205,46 @@ __device__ __forceinline__ void stats_piece(const unsigned char* slot, int ne, i
   c_out = (m == -INFINITY) ? -INFINITY : c;
 }
 
-// residual (or p) mass of one residual piece: target at slot[0..], draft at slot[2048..]
-__device__ __forceinline__ float resid_piece(const unsigned char* slot, const StageMeta& m,
-                                             int bf16, int lane) {
+// fp32 bits of element xl (0 <= xl < ne) of the piece, on every lane
+__device__ __forceinline__ uint32_t piece_element(const uint4 (&r)[4], int xl, int bf16, int lane) {
+  const int vx = bf16 ? (xl >> 3) : (xl >> 2);
+  const int owner = vx & 31, iv = vx >> 5, e = bf16 ? (xl & 7) : (xl & 3);
+  uint32_t out = 0;
+  if (lane == owner) {
+    uint4 vv = r[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+      if (i == iv) vv = r[i];
+    const int wi = bf16 ? (e >> 1) : e;
+    const uint32_t w = wi == 0 ? vv.x : wi == 1 ? vv.y : wi == 2 ? vv.z : vv.w;
+    out = bf16 ? ((e & 1) ? (w & 0xFFFF0000u) : (w << 16)) : w;
+  }
+  return __shfl_sync(0xffffffffu, out, owner);
+}
+
+// residual (or p) mass of a piece held in registers
+__device__ __forceinline__ float piece_resid(const uint4 (&t)[4], const uint4 (&d)[4], int bf16,
+                                             const StopInfo& st) {
   float acc = 0.f;
-  const int epv = bf16 ? 8 : 4;
-  const int nv = (m.ne + epv - 1) / epv;
-  const uint4* tv = reinterpret_cast<const uint4*>(slot);
-  const uint4* dv = reinterpret_cast<const uint4*>(slot + kResidRowBytes);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const int vi = lane + 32 * i;
-    if (vi >= nv) continue;
-    const uint4 t4 = tv[vi];
-    const uint4 d4 = (m.mode == 0) ? dv[vi] : make_uint4(0, 0, 0, 0);
-    const uint32_t* tw = reinterpret_cast<const uint32_t*>(&t4);
-    const uint32_t* dw = reinterpret_cast<const uint32_t*>(&d4);
-    const int rem = m.ne - vi * epv;
+    const uint32_t tw[4] = {t[i].x, t[i].y, t[i].z, t[i].w};
+    const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
     if (bf16) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        if (e < rem) {
-          const float t = (e & 1) ? bf16_hi(tw[e >> 1]) : bf16_lo(tw[e >> 1]);
-          const float d = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
-          acc += resid_val(t, d, m.ct, m.cd, m.invSt, m.invSd, m.mode);
-        }
+        const float tv = (e & 1) ? bf16_hi(tw[e >> 1]) : bf16_lo(tw[e >> 1]);
+        const float dv = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
+        acc += resid_val(tv, dv, st.ct, st.cd, st.invSt, st.invSd, st.mode);
       }
     } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (e < rem)
-          acc += resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), m.ct, m.cd, m.invSt,
-                           m.invSd, m.mode);
-      }
+      for (int e = 0; e < 4; ++e)
+        acc += resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), st.ct, st.cd, st.invSt,
+                         st.invSd, st.mode);
     }
   }
   return warp_sum(acc);
-}
-
-// ---------------------------------------------------------------------------
-// hand-offs: position -> row -> residual -> token
-// ---------------------------------------------------------------------------
-// Last statistics unit of row b: combine every position's unit partials, run
-// all accept tests (lane j = position j), find the first rejection n
-// and publish the stop constants.  The row's partials are staged through a
-// 4 KB shared-memory scratch with one cooperative load per round, so the
-// whole hand-off costs a few global round trips.
-constexpr int kFinScratch = 128;  // unit partials (4 KB)
-
-__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
-               "l"(gmem_src)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 __device__ __forceinline__ void combine_part(const UnitPart& u, float& Ct, ff& St, float& Cd,
@@ -699,75 +264,63 @@ __device__ __forceinline__ void combine_part(const UnitPart& u, float& Ct, ff& S
   }
 }
 
-__device__ void finalize_row(const DenseParams& P, int b, int lane, UnitPart* scr) {
-  fence_acq_rel_gpu();
-  const int G = P.G, nc = P.g.nc_s;
+// warp-wide combination of per-lane (C, S) pairs
+__device__ __forceinline__ void warp_combine(float& C, ff& S) {
+  const float Cw = warp_max(C);
+  S = warp_sum_ff(ff_mul_f(S, part_scale(C, Cw)));
+  C = Cw;
+}
+
+struct FinShared {
+  float c[4][kMaxG];  // per position: Ct, St, Cd, Sd (the stop position's constants)
+  int n;              // first rejected position (G + 1: none)
+  int err;
+};
+
+// Row b's decisions, by the CTA that completed its statistics (all warps).
+// Warp w combines the chunk partials of positions w, w + 16, ...; then the
+// first rejection n, the stop record and the outputs other than token n.
+__device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, FinShared& F) {
+  const int G = P.G, nc = P.g.nc;
   UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
-  // reserve the row's queue entries now; the result is needed only at the end
-  unsigned base = 0;
-  if (lane == 0) base = atomicAdd(&hdr_of(P)->rq_reserve, (unsigned)P.g.nc_r);
-  int n = G, err_any = 0, have_stop = 0;
-  float s_ct = 0.f, s_cd = 0.f, s_St = 1.f, s_Sd = 1.f;
-  for (int j0 = 0; j0 <= G; j0 += 32) {
-    const int j = j0 + lane;
-    const bool on = j <= G;
-    const int npos = min(32, G + 1 - j0);
-    int err = 0, x = 0;
-    float uacc = 0.f;
-    if (on && j < G) {
-      x = P.x[(size_t)b * G + j];
-      uacc = P.u_acc[(size_t)b * G + j];
-    }
+  if (threadIdx.x == 0) {
+    F.n = G + 1;
+    F.err = 0;
+  }
+  __syncthreads();
+  for (int j = warp; j <= G; j += kWarps) {
     float Ct = -INFINITY, Cd = -INFINITY;
     ff St{0.f, 0.f}, Sd{0.f, 0.f};
-    const int kstep = max(1, kFinScratch / npos);
-    bool gathered = false;
-    float tx = 0.f, dx = 0.f;
-    for (int k0 = 0; k0 < nc; k0 += kstep) {
-      const int kn = min(kstep, nc - k0);
-      const int total = npos * kn;  // <= kFinScratch
-      // cooperative copy of this round's partials into the scratch: every
-      // copy in flight at once (cp.async, no registers), then zero the source
-      __syncwarp();  // the previous round's reads of the scratch are done
-      for (int f = lane; f < total; f += 32) {
-        const int pp = f / kn, kk = f - pp * kn;
-        const unsigned char* q =
-            reinterpret_cast<const unsigned char*>(up_row + (size_t)(j0 + pp) * nc + k0 + kk);
-        cp_async16(scr + f, q);
-        cp_async16(reinterpret_cast<unsigned char*>(scr + f) + 16, q + 16);
+    uint32_t txb = kNoTokenBits, dxb = kNoTokenBits;
+    for (int k = lane; k < nc; k += 32) {
+      UnitPart* q = up_row + (size_t)j * nc + k;
+      const UnitPart u = ldcg32(q);
+      zero32(q);  // consumed: leave the workspace zero
+      combine_part(u, Ct, St, Cd, Sd);
+      if (__float_as_uint(u.tx) != kNoTokenBits) {
+        txb = __float_as_uint(u.tx);
+        dxb = __float_as_uint(u.dx);
       }
-      if (!gathered) {  // the gather at the draft token, overlapping the copies
-        gathered = true;
-        if (on && j < G) {
-          if (x < 0 || x >= P.V) {
-            err = 1;
-          } else {
-            tx = load_logit(target_row(P, b, j), x, P.bf16);
-            dx = load_logit(draft_row(P, b, j), x, P.bf16);
-          }
-        }
-      }
-      cp_async_wait_all();
-      for (int f = lane; f < total; f += 32) {  // consumed: leave the workspace zero
-        const int pp = f / kn, kk = f - pp * kn;
-        int4* q = reinterpret_cast<int4*>(up_row + (size_t)(j0 + pp) * nc + k0 + kk);
-        q[0] = make_int4(0, 0, 0, 0);
-        q[1] = make_int4(0, 0, 0, 0);
-      }
-      __syncwarp();
-      if (on)
-        for (int k = 0; k < kn; ++k) combine_part(scr[lane * kn + k], Ct, St, Cd, Sd);
+    }
+    warp_combine(Ct, St);
+    warp_combine(Cd, Sd);
+    const unsigned hx = __ballot_sync(0xffffffffu, txb != kNoTokenBits);
+    if (hx) {
+      txb = __shfl_sync(0xffffffffu, txb, __ffs(hx) - 1);
+      dxb = __shfl_sync(0xffffffffu, dxb, __ffs(hx) - 1);
     }
     const float Stf = ff_to_f(St), Sdf = ff_to_f(Sd);
-    if (on) {
-      err |= !(Ct > -INFINITY && Ct < INFINITY && Stf > 0.f && Stf < INFINITY);
-      if (j < G) err |= !(Cd > -INFINITY && Cd < INFINITY && Sdf > 0.f && Sdf < INFINITY);
+    int err = !(Ct > -INFINITY && Ct < INFINITY && Stf > 0.f && Stf < INFINITY);
+    if (j < G) {
+      err |= !(Cd > -INFINITY && Cd < INFINITY && Sdf > 0.f && Sdf < INFINITY);
+      err |= !hx;  // no chunk held x_j: the draft id is out of range
     }
     int acc = 1;
     float a = 0.f;
-    if (on && j < G && !err) {
+    if (j < G && !err) {
       // p/q = 2^((tx L - Ct) - (dx L - Cd)) * (Sd / St); the exponent is formed
       // exactly (two-product) and rounded once
+      const float tx = __uint_as_float(txb), dx = __uint_as_float(dxb);
       float ratio = 0.f;
       if (tx > -INFINITY && dx > -INFINITY) {
         const ff ea = ff_add_f(two_prod(tx, kLog2e), -Ct);
@@ -775,63 +328,143 @@ __device__ void finalize_row(const DenseParams& P, int b, int lane, UnitPart* sc
         ratio = exp2f(ff_to_f(ff_sub(ea, ed))) * __fdiv_rn(Sdf, Stf);
       }
       a = fminf(ratio, 1.f);
-      acc = uacc < a;
+      acc = P.u_acc[(size_t)b * G + j] < a;
     }
-    if (on && j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
-    err_any |= __any_sync(0xffffffffu, on && err);
-    const unsigned rej = __ballot_sync(0xffffffffu, on && j < G && !acc);
-    int src = -1;
-    if (!have_stop && rej) {
-      n = j0 + __ffs(rej) - 1;
-      src = n - j0;
-    } else if (!have_stop && G <= j0 + 31) {
-      src = G - j0;  // no rejection anywhere: the bonus position
-    }
-    if (src >= 0) {
-      have_stop = 1;
-      s_ct = __shfl_sync(0xffffffffu, Ct, src);
-      s_cd = __shfl_sync(0xffffffffu, Cd, src);
-      s_St = __shfl_sync(0xffffffffu, Stf, src);
-      s_Sd = __shfl_sync(0xffffffffu, Sdf, src);
+    if (lane == 0) {
+      if (j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
+      F.c[0][j] = Ct;
+      F.c[1][j] = Stf;
+      F.c[2][j] = Cd;
+      F.c[3][j] = Sdf;
+      if (err) atomicOr(&F.err, 1);
+      if (!acc) atomicMin(&F.n, j);
     }
   }
-  if (lane == 0) {
+  __syncthreads();
+  const int err = F.err;
+  const int n = min(F.n, G);
+  if (threadIdx.x == 0) {
     StopInfo st;
     st.n = n;
     st.T = 0.0;
-    if (err_any) {
+    if (err) {
       st.mode = 2;
       st.ct = st.cd = st.invSt = st.invSd = 0.f;
       atomicOr(&hdr_of(P)->status, kStatusInputErr);
     } else if (n < G) {
       st.mode = 0;
-      st.ct = s_ct;
-      st.cd = s_cd;
-      st.invSt = __fdiv_rn(1.f, s_St);
-      st.invSd = __fdiv_rn(1.f, s_Sd);
+      st.ct = F.c[0][n];
+      st.cd = F.c[2][n];
+      st.invSt = __fdiv_rn(1.f, F.c[1][n]);
+      st.invSd = __fdiv_rn(1.f, F.c[3][n]);
     } else {
       st.mode = 1;
-      st.ct = s_ct;
+      st.ct = F.c[0][n];
       st.cd = 0.f;
-      st.invSt = __fdiv_rn(1.f, s_St);
+      st.invSt = __fdiv_rn(1.f, F.c[1][n]);
       st.invSd = 0.f;
     }
     ws_at<StopInfo>(P, P.L.stop)[b] = st;
     ws_at<uint32_t>(P, P.L.cnt_row)[b] = 0;
-    fence_acq_rel_gpu();
+    P.n_out[b] = err ? -1 : n;
   }
-  // publish the row's residual units to the queue
-  base = __shfl_sync(0xffffffffu, base, 0);
-  __syncwarp();
-  for (int c = lane; c < P.g.nc_r; c += 32)
-    st_release_u64(rq_of(P) + base + c, ((unsigned long long)(b + 1) << 32) | (unsigned)c);
-  __syncwarp();
+  // tokens: x_0..x_{n-1}, then (token n from the residual kernel), then -1
+  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
+  for (int j = threadIdx.x; j <= G; j += kThreads) {
+    if (err)
+      tok[j] = -1;
+    else if (j < n)
+      tok[j] = P.x[(size_t)b * G + j];
+    else if (j > n)
+      tok[j] = -1;
+  }
 }
 
-// Select the token of row b from its per-piece masses (float-float prefix over
-// pieces, then over the fp32 element values of the chosen piece).  The
-// masses, then the chosen piece's logits, are staged in the shared scratch
-// with cp.async: two global round trips.
+// ---------------------------------------------------------------------------
+// kernel 1: statistics of one 32 KB chunk of (row b, position j), target and
+// draft; the CTA completing a row finalises it
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 2) dense_stats_kernel(const __grid_constant__ DenseParams P) {
+  __shared__ float s_c[2][kWarps], s_s[2][kWarps];
+  __shared__ uint32_t s_x[2];
+  __shared__ int s_last;
+  __shared__ FinShared F;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = P.G, nc = P.g.nc, pe = P.g.pe;
+  const long long t = blockIdx.x;
+  const long long r = t / nc;
+  const int c = (int)(t - r * nc);
+  const int b = (int)(r / (G + 1));
+  const int j = (int)(r - (long long)b * (G + 1));
+  const bool has_d = j < G;
+  const int k = c * kWarps + warp;  // this warp's piece
+  const int ne = (k < P.g.np) ? min(pe, P.V - k * pe) : 0;
+  const int x = has_d ? __ldg(P.x + (size_t)b * G + j) : -1;
+  if (threadIdx.x < 2) s_x[threadIdx.x] = kNoTokenBits;
+
+  uint4 rt[4], rd[4];
+  const size_t off = (size_t)k * kPieceBytes;
+  load_piece(target_row(P, b, j) + off, ne, P.bf16, P.aligned, lane, rt);
+  if (has_d) {
+    load_piece(draft_row(P, b, j) + off, ne, P.bf16, P.aligned, lane, rd);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) rd[i] = make_uint4(0, 0, 0, 0);
+  }
+  float ct, st, cd = -INFINITY, sd = 0.f;
+  piece_stats(rt, P.bf16, ct, st);
+  if (has_d) piece_stats(rd, P.bf16, cd, sd);
+  // the logits at the draft token, if this piece holds it
+  const int xl = x - k * pe;
+  if (has_d && xl >= 0 && xl < ne) {
+    const uint32_t tb = piece_element(rt, xl, P.bf16, lane);
+    const uint32_t db = piece_element(rd, xl, P.bf16, lane);
+    if (lane == 0) {
+      s_x[0] = tb;
+      s_x[1] = db;
+    }
+  }
+  if (lane == 0) {
+    s_c[0][warp] = ct;
+    s_s[0][warp] = st;
+    s_c[1][warp] = cd;
+    s_s[1][warp] = sd;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const bool on = lane < kWarps;
+    float Ct = on ? s_c[0][lane] : -INFINITY, Cd = on ? s_c[1][lane] : -INFINITY;
+    ff St{on ? s_s[0][lane] : 0.f, 0.f}, Sd{on ? s_s[1][lane] : 0.f, 0.f};
+    warp_combine(Ct, St);
+    warp_combine(Cd, Sd);
+    if (lane == 0) {
+      UnitPart u;
+      u.St_hi = St.hi;
+      u.St_lo = St.lo;
+      u.Sd_hi = Sd.hi;
+      u.Sd_lo = Sd.lo;
+      u.ct = Ct;
+      u.cd = Cd;
+      u.tx = __uint_as_float(s_x[0]);
+      u.dx = __uint_as_float(s_x[1]);
+      ws_at<UnitPart>(P, P.L.upart)[((size_t)b * (G + 1) + j) * nc + c] = u;
+      __threadfence();
+      const unsigned old = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + b, 1u);
+      s_last = (old == (unsigned)((G + 1) * nc) - 1);
+    }
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // every chunk's partial is visible before it is read
+  finalize_row(P, b, warp, lane, F);
+}
+
+// ---------------------------------------------------------------------------
+// token draw of row b from its per-piece masses (one warp): a float-float
+// prefix over the pieces picks the piece, a float-float prefix over its fp32
+// element values picks the token.  Masses, then the piece's two slices, are
+// staged in the shared scratch with cp.async.
+// ---------------------------------------------------------------------------
 template <int BF16>
 __device__ __forceinline__ float piece_val(const float* tsm, const float* dsm, int e,
                                            const StopInfo& st) {
@@ -846,21 +479,19 @@ __device__ __forceinline__ float piece_val(const float* tsm, const float* dsm, i
   return resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
 }
 
+constexpr int kScrFloats = 1024;  // 4 KB: the masses, or one piece's two slices
+
 template <int BF16>
 __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) {
-  fence_acq_rel_gpu();
-  const int G = P.G, V = P.V, np = P.g.np_r, re = P.g.re;
-  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np_r4;
-  constexpr int kScrFloats = 1024;  // 4 KB
+  const int G = P.G, V = P.V, np = P.g.np, pe = P.g.pe;
+  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
   const bool staged = np <= kScrFloats;
   // the mass copies and the stop-record load are in flight together
   if (staged)
     for (int k = lane * 4; k < np; k += 128) cp_async16(scr + k, rm + k);
   StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
   const float us = P.u_s[b];
-  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
   const int n = st.n;
-  int y = -1;
   ff T{0.f, 0.f};
   cp_async_wait_all();
   __syncwarp();
@@ -871,7 +502,7 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
     const int per = (np + 31) / 32;
     const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
     ff ls{0.f, 0.f};
-    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, mv[k]);
+    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, staged ? mv[k] : __ldcg(mv + k));
     ff ex = warp_exclusive_scan_ff(ls, lane);
     T = ff_shfl(ff_add(ex, ls), 31);
     if (!(T.hi > 0.f) && st.mode == 0) {
@@ -879,7 +510,7 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
       st.mode = 1;
       drow = nullptr;
       for (int k = 0; k < np; ++k) {
-        const int y0 = k * re, ne = min(re, V - y0);
+        const int y0 = k * pe, ne = min(pe, V - y0);
         float sum = 0.f;
         for (int e = lane; e < ne; e += 32)
           sum += resid_val(load_logit(trow, y0 + e, BF16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
@@ -891,7 +522,7 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
             rm[k] = sum;
         }
       }
-      fence_acq_rel_gpu();
+      __threadfence();
       __syncwarp();
       ls = ff{0.f, 0.f};
       for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, staged ? scr[k] : __ldcg(rm + k));
@@ -933,11 +564,9 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
       kstar = last < 0 ? 0 : last;
     }
-    // the masses are consumed: leave the workspace zero for the next call
-    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
     __syncwarp();
     // element level within piece kstar: stage its target and draft slices
-    const int y0 = kstar * re, ne = min(re, V - y0);
+    const int y0 = kstar * pe, ne = min(pe, V - y0);
     const float* tsm = scr;
     const float* dsm = scr + 512;  // 2 KB in
     if (P.aligned) {
@@ -969,14 +598,15 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
     ff es{0.f, 0.f};
     int lastpos = -1;
     for (int e = e0; e < e1; ++e) {
-      const float r = piece_val<BF16>(tsm, dsm, e, st);
-      es = ff_add_f(es, r);
-      if (r > 0.f) lastpos = e;
+      const float rv = piece_val<BF16>(tsm, dsm, e, st);
+      es = ff_add_f(es, rv);
+      if (rv > 0.f) lastpos = e;
     }
     const ff eex = warp_exclusive_scan_ff(es, lane);
     const ff tl = ff_sub(target, base);
     const unsigned ehit =
         clamp ? 0u : __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(eex, es), tl));
+    int y;
     if (ehit) {
       const int fl = __ffs(ehit) - 1;
       int yy = -1;
@@ -997,26 +627,17 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
       for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
       y = y0 + (lp < 0 ? 0 : lp);
     }
+    if (lane == 0) P.tok_out[(size_t)b * (G + 1) + n] = y;
   }
-  if (st.mode == 2)  // an error row never reached the piece-level search
-    for (int k = lane; k < np; k += 32) rm[k] = 0.f;
-  // outputs
-  const int nn = (st.mode == 2) ? -1 : n;
-  for (int j = lane; j <= G; j += 32) {
-    int v = -1;
-    if (nn >= 0) v = (j < nn) ? P.x[(size_t)b * G + j] : (j == nn ? y : -1);
-    tok[j] = v;
-  }
+  // the masses are consumed: leave the workspace zero
+  for (int k = lane; k < np; k += 32) rm[k] = 0.f;
   if (lane == 0) {
-    P.n_out[b] = nn;
     StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
     if (P.keep_stop) {  // read (and cleared) by the residual-output kernel
       sp->mode = st.mode;
       sp->T = (double)T.hi + (double)T.lo;
     } else {
-      int4* qq = reinterpret_cast<int4*>(sp);
-      qq[0] = make_int4(0, 0, 0, 0);
-      qq[1] = make_int4(0, 0, 0, 0);
+      zero32(sp);
     }
     ws_at<uint32_t>(P, P.L.cnt_res)[b] = 0;
   }
@@ -1024,213 +645,48 @@ __device__ void final_select(const DenseParams& P, int b, int lane, float* scr) 
 }
 
 // ---------------------------------------------------------------------------
-// consumer loop
+// kernel 2: residual (or p) masses of one 32 KB chunk of the stop position's
+// rows, one per piece; the CTA completing a row draws its token
 // ---------------------------------------------------------------------------
-// queue a row hand-off for this CTA's finaliser warp (lane 0 of a consumer)
-template <int NS, int NW>
-__device__ __forceinline__ void fin_push(const DenseParams& P, Smem<NS, NW>& S, int item, int lane) {
-  if (lane == 0) {
-    const unsigned pos = atomicAdd(&S.fin_tail, 1u);
-    // the queue has kFinQ entries; wait (bounded) while it is full
-    const long long t0 = clock64();
-    while (pos - *reinterpret_cast<volatile unsigned*>(&S.fin_head) >= (unsigned)kFinQ) {
-      if (clock64() - t0 > P.wait_bound) {
-        record_timeout(P, kSiteFinPush, pos);
-        break;
-      }
-      nanosleep_ns(32);
-    }
-    S.fin_item[pos % kFinQ] = item;
-    __threadfence_block();
-    *reinterpret_cast<volatile unsigned*>(&S.fin_seq[pos % kFinQ]) = pos + 1;
-  }
-  __syncwarp();
-}
-template <int NS, int NW>
-__device__ void consumer(const DenseParams& P, Smem<NS, NW>& S, int cw, int lane) {
-  const int G = P.G;
-  for (uint32_t s = cw;; s += NW) {
-    const int slot = s % NS;
-    if (!wait_phase(&S.full[slot], (s / NS) & 1, P, kSiteConsFull, s)) break;
-    const StageMeta m = S.meta[slot];
-    if (m.kind == kEnd) break;
-    UnitSlot& U = S.unit[m.uslot];
-    auto release = [&]() {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.empty[slot]);
-    };
-    if (m.kind == kStatsT || m.kind == kStatsD) {
-      float c, sm;
-      stats_piece(S.ring[slot], m.ne, P.bf16, lane, c, sm, release);
-      unsigned old = 0;
-      if (lane == 0) {
-        U.c[m.pidx] = c;
-        U.s[m.pidx] = sm;
-        __threadfence_block();
-        old = atomicAdd(&U.count, 1u);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      int row_done = 0;
-      if (old == (unsigned)m.upieces - 1) {
-        __threadfence_block();
-        __syncwarp();
-        const bool have = lane < m.upieces;
-        const bool isd = lane >= m.npc;
-        const float cl = have ? U.c[lane] : -INFINITY;
-        const float sl = have ? U.s[lane] : 0.f;
-        const float Ct = warp_max((have && !isd) ? cl : -INFINITY);
-        const float Cd = warp_max((have && isd) ? cl : -INFINITY);
-        const ff wt = (have && !isd) ? two_prod(sl, part_scale(cl, Ct)) : ff{0.f, 0.f};
-        const ff wd = (have && isd) ? two_prod(sl, part_scale(cl, Cd)) : ff{0.f, 0.f};
-        const ff St = warp_sum_ff(wt), Sd = warp_sum_ff(wd);
-        if (lane == 0) {
-          U.count = 0;
-          mbar_arrive(&S.ufree[m.uslot]);
-          UnitPart u;
-          u.St_hi = St.hi;
-          u.St_lo = St.lo;
-          u.Sd_hi = Sd.hi;
-          u.Sd_lo = Sd.lo;
-          u.ct = Ct;
-          u.cd = Cd;
-          u.pad[0] = u.pad[1] = 0.f;
-          ws_at<UnitPart>(P, P.L.upart)[((size_t)m.b * (G + 1) + m.j) * P.g.nc_s + m.unit_c] = u;
-          fence_acq_rel_gpu();
-          const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + m.b, 1u);
-          row_done = (o2 == (unsigned)((G + 1) * P.g.nc_s) - 1);
-        }
-        row_done = __shfl_sync(0xffffffffu, row_done, 0);
-      }
-      if (row_done) fin_push(P, S, m.b + 1, lane);
-    } else {
-      const float mass = (m.kind == kResid) ? resid_piece(S.ring[slot], m, P.bf16, lane) : 0.f;
-      release();
-      unsigned old = 0;
-      if (lane == 0) {
-        U.s[m.pidx] = mass;
-        __threadfence_block();
-        old = atomicAdd(&U.count, 1u);
-      }
-      old = __shfl_sync(0xffffffffu, old, 0);
-      int row_done = 0;
-      if (lane == 0 && old == (unsigned)m.upieces - 1) {
-        __threadfence_block();
-        float* rm = ws_at<float>(P, P.L.rmass) + (size_t)m.b * P.g.np_r4 + m.unit_c * kUnitPieces;
-        for (int k = 0; k < m.upieces; ++k) rm[k] = U.s[k];
-        U.count = 0;
-        mbar_arrive(&S.ufree[m.uslot]);
-        fence_acq_rel_gpu();
-        const unsigned o2 = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_res) + m.b, 1u);
-        row_done = (o2 == (unsigned)P.g.nc_r - 1);
-      }
-      row_done = __shfl_sync(0xffffffffu, row_done, 0);
-      if (row_done) fin_push(P, S, -(m.b + 1), lane);
-    }
-  }
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    atomicAdd(&S.cons_done, 1u);
-  }
-}
-
-// finaliser warp: runs the row hand-offs the consumers queue, in order
-template <int NS, int NW>
-__device__ void finaliser(const DenseParams& P, Smem<NS, NW>& S, int lane) {
-  WsHeader* h = hdr_of(P);
-  unsigned head = 0;
-  long long t0 = clock64();
-  for (;;) {
-    int item = 0, state = 0;  // state 1: item, 2: done, 3: timeout/abort
-    if (lane == 0) {
-      const volatile unsigned* seq = S.fin_seq;
-      if (seq[head % kFinQ] == head + 1) {
-        __threadfence_block();
-        item = S.fin_item[head % kFinQ];
-        state = 1;
-      } else if (*reinterpret_cast<volatile unsigned*>(&S.cons_done) == (unsigned)NW &&
-                 *reinterpret_cast<volatile unsigned*>(&S.fin_tail) == head) {
-        state = 2;
-      } else if (*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
-        state = 3;
-      } else if (clock64() - t0 > 4 * P.wait_bound) {
-        // the finaliser only waits on its own CTA, whose waits have the
-        // shorter bound: a longer one here lets the root cause report first
-        record_timeout(P, kSiteFinIdle, head);
-        state = 3;
-      } else {
-        nanosleep_ns(256);
-      }
-    }
-    state = __shfl_sync(0xffffffffu, state, 0);
-    if (state >= 2) break;
-    if (state == 0) continue;
-    item = __shfl_sync(0xffffffffu, item, 0);
-    __syncwarp();
-    if (item > 0) {
-      finalize_row(P, item - 1, lane, S.fin_scratch);
-    } else if (P.bf16) {
-      final_select<1>(P, -item - 1, lane, reinterpret_cast<float*>(S.fin_scratch));
-    } else {
-      final_select<0>(P, -item - 1, lane, reinterpret_cast<float*>(S.fin_scratch));
-    }
-    ++head;
-    if (lane == 0) *reinterpret_cast<volatile unsigned*>(&S.fin_head) = head;
-    t0 = clock64();
-  }
-}
-
-// register budget: each of the SM's four sub-partitions has 16K registers and
-// holds ceil(warps / 4) of the resident warps
-template <int NW, int CTAS>
-constexpr int dense_regs() {
-  constexpr int per_part = ((NW + 2) * CTAS + 3) / 4;
-  constexpr int r = 16384 / (32 * per_part) / 8 * 8;
-  return r > 255 ? 255 : r;
-}
-
-template <int NS, int NW, int CTAS>
-__global__ void __maxnreg__((dense_regs<NW, CTAS>()))
-    dense_verify_kernel(const __grid_constant__ DenseParams P) {
-  extern __shared__ __align__(1024) unsigned char smem_raw[];
-  using SM = Smem<NS, NW>;
-  SM& S = *reinterpret_cast<SM*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, 2) dense_resid_kernel(const __grid_constant__ DenseParams P) {
+  __shared__ __align__(16) float scr[kScrFloats];
+  __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NS; ++i) {
-      mbar_init(&S.full[i], 1);
-      mbar_init(&S.empty[i], 1);
+  const int nc = P.g.nc, pe = P.g.pe;
+  const int b = (int)(blockIdx.x / nc);
+  const int c = (int)(blockIdx.x - (long long)b * nc);
+  const int k = c * kWarps + warp;
+  const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
+  if (k < P.g.np) {
+    float mass = 0.f;
+    if (st.mode != 2) {
+      const int ne = min(pe, P.V - k * pe);
+      const size_t off = (size_t)k * kPieceBytes;
+      uint4 rt[4], rd[4];
+      load_piece(target_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rt);
+      if (st.mode == 0) {
+        load_piece(draft_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rd);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) rd[i] = rt[i];  // unused by mode 1
+      }
+      mass = piece_resid(rt, rd, P.bf16, st);
     }
-    for (int i = 0; i < SM::NU; ++i) {
-      mbar_init(&S.ufree[i], 1);
-      S.unit[i].count = 0;
-    }
-    for (int i = 0; i < kFinQ; ++i) S.fin_seq[i] = 0u;
-    S.fin_tail = S.fin_head = S.cons_done = 0u;
-    fence_mbar_init();
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
   }
   __syncthreads();
-  if (warp == 0)
-    producer(P, S, lane);
-  else if (warp <= NW)
-    consumer(P, S, warp - 1, lane);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned old = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_res) + b, 1u);
+    s_last = (old == (unsigned)nc - 1);
+  }
+  __syncthreads();
+  if (!s_last || warp != 0) return;
+  __threadfence();  // every chunk's masses are visible before they are read
+  if (P.bf16)
+    final_select<1>(P, b, lane, scr);
   else
-    finaliser(P, S, lane);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    WsHeader* h = hdr_of(P);
-    fence_acq_rel_gpu();
-    const unsigned prev = atomicAdd(&h->exit_cnt, 1u);
-    // after a timeout the counters are left as they are, for diagnosis
-    if (prev == gridDim.x - 1 && !*reinterpret_cast<volatile uint32_t*>(&h->abort)) {
-      h->ticket = 0ull;
-      h->rq_head = 0u;
-      h->rq_reserve = 0u;
-      h->exit_cnt = 0u;
-      fence_acq_rel_gpu();
-    }
-  }
+    final_select<0>(P, b, lane, scr);
 }
 
 // residual_out: the distribution the emitted token was drawn from.  One CTA
@@ -1240,11 +696,7 @@ __global__ void dense_resid_out_kernel(const __grid_constant__ DenseParams P, fl
   StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
   const StopInfo st = ldcg32(sp);
   __syncthreads();
-  if (threadIdx.x == 0) {
-    int4* q = reinterpret_cast<int4*>(sp);
-    q[0] = make_int4(0, 0, 0, 0);
-    q[1] = make_int4(0, 0, 0, 0);
-  }
+  if (threadIdx.x == 0) zero32(sp);
   float* o = out + (size_t)b * P.V;
   if (st.mode == 2 || !(st.T > 0.0)) {
     for (int y = threadIdx.x; y < P.V; y += blockDim.x) o[y] = 0.f;
@@ -1260,48 +712,15 @@ __global__ void dense_resid_out_kernel(const __grid_constant__ DenseParams P, fl
   }
 }
 
-// kernel configurations: ring stages, consumer warps, CTAs per SM
-struct DenseConfig {
-  void (*fn)(DenseParams);
-  size_t smem;
-  int threads;
-  int ctas_per_sm;
-};
-
-template <int NS, int NW, int CTAS>
-DenseConfig make_config() {
-  DenseConfig c;
-  c.fn = dense_verify_kernel<NS, NW, CTAS>;
-  c.smem = sizeof(Smem<NS, NW>);
-  c.threads = 32 * (NW + 2);
-  c.ctas_per_sm = CTAS;
-  return c;
-}
-
-const DenseConfig& active_config() {
-  // 2 CTAs per SM, 24-stage rings, 8 consumer warps each (measured fastest of
-  // the configurations whose ring depth is a multiple of the consumer warps)
-  static const DenseConfig cfg = make_config<24, 8, 2>();
-  return cfg;
-}
-
 }  // namespace
 
-size_t dense_smem_bytes() { return active_config().smem; }
-int dense_ctas_per_sm() { return active_config().ctas_per_sm; }
-
-cudaError_t launch_dense(const DenseParams& p, int grid, cudaStream_t s) {
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
+  const long long g1 = (long long)p.B * (p.G + 1) * p.g.nc;
+  const long long g2 = (long long)p.B * p.g.nc;
+  dense_stats_kernel<<<(unsigned)g1, kThreads, 0, s>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const DenseConfig& c = active_config();
-  if (dev < 0 || dev >= 64 || !configured[dev]) {
-    e = cudaFuncSetAttribute(c.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) configured[dev] = true;
-  }
-  c.fn<<<grid, c.threads, c.smem, s>>>(p);
+  dense_resid_kernel<<<(unsigned)g2, kThreads, 0, s>>>(p);
   return cudaGetLastError();
 }
 
