@@ -93,8 +93,8 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
   const sv::DenseGeom g = sv::dense_geom(V, es);
   const sv::DenseLayout L = sv::dense_layout(B, gamma, g);
   if (ws_bytes < L.total) return SV_ERR_INVALID_ARG;
-  // one CTA per (row, position, chunk) and per (row, chunk): 31-bit grids
-  if ((long long)B * (gamma + 1) * g.nc >= (1ll << 31) - 1) return SV_ERR_INVALID_ARG;
+  // pieces are numbered with 31-bit indices in places
+  if ((long long)B * (gamma + 1) * g.np >= (1ll << 31) - 1) return SV_ERR_INVALID_ARG;
   sv::DenseParams p;
   memset(&p, 0, sizeof p);
   p.lt = static_cast<const unsigned char*>(target_logits);

@@ -105,9 +105,6 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
                "l"(gmem_src)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.wait_all;" ::: "memory");
-}
 
 // streaming 16-byte load: no L1 allocation (every byte is read once here)
 __device__ __forceinline__ uint4 ld_stream(const void* p) {
@@ -275,13 +272,16 @@ struct FinShared {
   float c[4][kMaxG];  // per position: Ct, St, Cd, Sd (the stop position's constants)
   int n;              // first rejected position (G + 1: none)
   int err;
+  StopInfo st;        // the result: stop position and its draw constants
 };
 
-// Row b's decisions, by the CTA that completed its statistics (all warps).
-// Warp w combines the chunk partials of positions w, w + 16, ...; then the
-// first rejection n, the stop record and the outputs other than token n.
-__device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, FinShared& F) {
-  const int G = P.G, nc = P.g.nc;
+// Row b's decisions (all warps of the CTA).  Warp w combines the segment
+// records of positions w, w + 16, ...; then the first rejection n and the draw
+// constants (F.st).  The owner also writes the accept probabilities, n and
+// every token but token n.
+__device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, FinShared& F,
+                             bool owner) {
+  const int G = P.G, nc = P.g.np;  // one record per piece
   UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
   if (threadIdx.x == 0) {
     F.n = G + 1;
@@ -292,14 +292,24 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     float Ct = -INFINITY, Cd = -INFINITY;
     ff St{0.f, 0.f}, Sd{0.f, 0.f};
     uint32_t txb = kNoTokenBits, dxb = kNoTokenBits;
-    for (int k = lane; k < nc; k += 32) {
-      UnitPart* q = up_row + (size_t)j * nc + k;
-      const UnitPart u = ldcg32(q);
-      zero32(q);  // consumed: leave the workspace zero
-      combine_part(u, Ct, St, Cd, Sd);
-      if (__float_as_uint(u.tx) != kNoTokenBits) {
-        txb = __float_as_uint(u.tx);
-        dxb = __float_as_uint(u.dx);
+    for (int k0 = 0; k0 < nc; k0 += 4 * 32) {
+      // four records per lane in flight at once, then zeroed, then combined
+      UnitPart u[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = k0 + lane + 32 * q;
+        if (k < nc) u[q] = ldcg32(up_row + (size_t)j * nc + k);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = k0 + lane + 32 * q;
+        if (k < nc && !(u[q].St_hi == 0.f && u[q].ct == 0.f)) {  // empty slots hold zeros
+          combine_part(u[q], Ct, St, Cd, Sd);
+          if (__float_as_uint(u[q].tx) != kNoTokenBits) {
+            txb = __float_as_uint(u[q].tx);
+            dxb = __float_as_uint(u[q].dx);
+          }
+        }
       }
     }
     warp_combine(Ct, St);
@@ -331,7 +341,8 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
       acc = P.u_acc[(size_t)b * G + j] < a;
     }
     if (lane == 0) {
-      if (j < G && P.acc_out) P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
+      if (owner && j < G && P.acc_out)
+        P.acc_out[(size_t)b * G + j] = err ? __int_as_float(0x7fc00000) : a;
       F.c[0][j] = Ct;
       F.c[1][j] = Stf;
       F.c[2][j] = Cd;
@@ -350,7 +361,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     if (err) {
       st.mode = 2;
       st.ct = st.cd = st.invSt = st.invSd = 0.f;
-      atomicOr(&hdr_of(P)->status, kStatusInputErr);
+      if (owner) atomicOr(&hdr_of(P)->status, kStatusInputErr);
     } else if (n < G) {
       st.mode = 0;
       st.ct = F.c[0][n];
@@ -364,11 +375,12 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
       st.invSt = __fdiv_rn(1.f, F.c[1][n]);
       st.invSd = 0.f;
     }
-    ws_at<StopInfo>(P, P.L.stop)[b] = st;
-    ws_at<uint32_t>(P, P.L.cnt_row)[b] = 0;
-    P.n_out[b] = err ? -1 : n;
+    F.st = st;
+    if (owner) P.n_out[b] = err ? -1 : n;
   }
-  // tokens: x_0..x_{n-1}, then (token n from the residual kernel), then -1
+  __syncthreads();
+  if (!owner) return;
+  // tokens: x_0..x_{n-1}, then (token n, drawn later), then -1
   int32_t* tok = P.tok_out + (size_t)b * (G + 1);
   for (int j = threadIdx.x; j <= G; j += kThreads) {
     if (err)
@@ -381,312 +393,451 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
 }
 
 // ---------------------------------------------------------------------------
-// kernel 1: statistics of one 32 KB chunk of (row b, position j), target and
-// draft; the CTA completing a row finalises it
+// kernel 1: statistics of every piece.  Work items are the pieces (b, j, k)
+// in row order; every warp of the persistent grid takes one contiguous range
+// of them and streams it through a private kStages-deep ring of 4 KB shared
+// stages (2 KB target piece + 2 KB draft piece), filled by cp.async 16-byte
+// copies: while one item is reduced, the next kStages - 1 are in flight.
+// Each lane copies, and later reads, only its own vectors, so the ring needs
+// no synchronisation beyond the lane's own cp.async groups.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2) dense_stats_kernel(const __grid_constant__ DenseParams P) {
-  __shared__ float s_c[2][kWarps], s_s[2][kWarps];
-  __shared__ uint32_t s_x[2];
-  __shared__ int s_last;
-  __shared__ FinShared F;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = P.G, nc = P.g.nc, pe = P.g.pe;
-  const long long t = blockIdx.x;
-  const long long r = t / nc;
-  const int c = (int)(t - r * nc);
-  const int b = (int)(r / (G + 1));
-  const int j = (int)(r - (long long)b * (G + 1));
-  const bool has_d = j < G;
-  const int k = c * kWarps + warp;  // this warp's piece
-  const int ne = (k < P.g.np) ? min(pe, P.V - k * pe) : 0;
-  const int x = has_d ? __ldg(P.x + (size_t)b * G + j) : -1;
-  if (threadIdx.x < 2) s_x[threadIdx.x] = kNoTokenBits;
+constexpr int kStages = 3;
+constexpr int kStageBytes = 2 * kPieceBytes;
+constexpr size_t kStatsSmem = (size_t)kWarps * kStages * kStageBytes;
 
-  uint4 rt[4], rd[4];
-  const size_t off = (size_t)k * kPieceBytes;
-  load_piece(target_row(P, b, j) + off, ne, P.bf16, P.aligned, lane, rt);
-  if (has_d) {
-    load_piece(draft_row(P, b, j) + off, ne, P.bf16, P.aligned, lane, rd);
-  } else {
+struct Item {  // piece k of row-position (b, j)
+  int b, j, k;
+};
+__device__ __forceinline__ Item item_at(long long w, int G, int np) {
+  const long long r = w / np;
+  Item it;
+  it.k = (int)(w - r * np);
+  it.b = (int)(r / (G + 1));
+  it.j = (int)(r - (long long)it.b * (G + 1));
+  return it;
+}
+__device__ __forceinline__ void item_next(Item& it, int G, int np) {
+  if (++it.k == np) {
+    it.k = 0;
+    if (++it.j == G + 1) {
+      it.j = 0;
+      ++it.b;
+    }
+  }
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// this lane's vectors of piece `it` (target, and draft for j < G) -> stage
+__device__ __forceinline__ void issue_item(const DenseParams& P, const Item& it,
+                                           unsigned char* stage, int lane) {
+  const int pe = P.g.pe, epv = P.bf16 ? 8 : 4;
+  const int ne = min(pe, P.V - it.k * pe);
+  const size_t off = (size_t)it.k * kPieceBytes;
+  const unsigned char* ts = target_row(P, it.b, it.j) + off;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) rd[i] = make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < 4; ++i) {
+    const int vi = lane + 32 * i;
+    if (vi * epv < ne) cp_async16(stage + 16 * vi, ts + 16 * vi);
   }
-  float ct, st, cd = -INFINITY, sd = 0.f;
-  piece_stats(rt, P.bf16, ct, st);
-  if (has_d) piece_stats(rd, P.bf16, cd, sd);
-  // the logits at the draft token, if this piece holds it
-  const int xl = x - k * pe;
-  if (has_d && xl >= 0 && xl < ne) {
-    const uint32_t tb = piece_element(rt, xl, P.bf16, lane);
-    const uint32_t db = piece_element(rd, xl, P.bf16, lane);
-    if (lane == 0) {
-      s_x[0] = tb;
-      s_x[1] = db;
+  if (it.j < P.G) {
+    const unsigned char* ds = draft_row(P, it.b, it.j) + off;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      if (vi * epv < ne) cp_async16(stage + kPieceBytes + 16 * vi, ds + 16 * vi);
     }
   }
-  if (lane == 0) {
-    s_c[0][warp] = ct;
-    s_s[0][warp] = st;
-    s_c[1][warp] = cd;
-    s_s[1][warp] = sd;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    const bool on = lane < kWarps;
-    float Ct = on ? s_c[0][lane] : -INFINITY, Cd = on ? s_c[1][lane] : -INFINITY;
-    ff St{on ? s_s[0][lane] : 0.f, 0.f}, Sd{on ? s_s[1][lane] : 0.f, 0.f};
-    warp_combine(Ct, St);
-    warp_combine(Cd, Sd);
-    if (lane == 0) {
-      UnitPart u;
-      u.St_hi = St.hi;
-      u.St_lo = St.lo;
-      u.Sd_hi = Sd.hi;
-      u.Sd_lo = Sd.lo;
-      u.ct = Ct;
-      u.cd = Cd;
-      u.tx = __uint_as_float(s_x[0]);
-      u.dx = __uint_as_float(s_x[1]);
-      ws_at<UnitPart>(P, P.L.upart)[((size_t)b * (G + 1) + j) * nc + c] = u;
-      __threadfence();
-      const unsigned old = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_row) + b, 1u);
-      s_last = (old == (unsigned)((G + 1) * nc) - 1);
-    }
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();  // every chunk's partial is visible before it is read
-  finalize_row(P, b, warp, lane, F);
 }
 
-// ---------------------------------------------------------------------------
-// token draw of row b from its per-piece masses (one warp): a float-float
-// prefix over the pieces picks the piece, a float-float prefix over its fp32
-// element values picks the token.  Masses, then the piece's two slices, are
-// staged in the shared scratch with cp.async.
-// ---------------------------------------------------------------------------
-template <int BF16>
-__device__ __forceinline__ float piece_val(const float* tsm, const float* dsm, int e,
-                                           const StopInfo& st) {
-  float t, d;
-  if (BF16) {
-    t = bf16_to_f32(reinterpret_cast<const uint16_t*>(tsm)[e]);
-    d = bf16_to_f32(reinterpret_cast<const uint16_t*>(dsm)[e]);
+// Running statistics of the (row, position) segment a warp is streaming: the
+// pieces of one segment are folded together (float-float) and written as one
+// record, in the slot of the segment's first piece; the other slots of the
+// segment stay zero ("empty": St = 0 and c = 0, which no real record has).
+struct SegAcc {
+  long long w0;  // record slot: the segment's first piece
+  int b, j;
+  float Ct, Cd;
+  ff St, Sd;
+  uint32_t tb, db;  // logits at the draft token, if a piece of the segment held it
+};
+
+__device__ __forceinline__ void seg_begin(SegAcc& a, const Item& it, long long w) {
+  a.w0 = w;
+  a.b = it.b;
+  a.j = it.j;
+  a.Ct = a.Cd = -INFINITY;
+  a.St = a.Sd = ff{0.f, 0.f};
+  a.tb = a.db = kNoTokenBits;
+}
+
+__device__ __forceinline__ void seg_write(const DenseParams& P, const SegAcc& a, int lane) {
+  if (lane == 0) {
+    float4* q = reinterpret_cast<float4*>(ws_at<UnitPart>(P, P.L.upart) + a.w0);
+    q[0] = make_float4(a.St.hi, a.St.lo, a.Sd.hi, a.Sd.lo);
+    q[1] = make_float4(a.Ct, a.Cd, __uint_as_float(a.tb), __uint_as_float(a.db));
+  }
+}
+
+// fold (c, s) of one piece into a running (C, S); the rescale factor is one
+// ex2.approx (relative error ~2^-22), 0 for an all -inf side
+__device__ __forceinline__ void fold(float c, float s, float& C, ff& S) {
+  if (c > C) {
+    S = ff_add(ff_mul_f(S, (C == -INFINITY) ? 0.f : ex2(C - c)), ff{s, 0.f});
+    C = c;
   } else {
-    t = tsm[e];
-    d = dsm[e];
+    S = ff_add(S, two_prod(s, (c == -INFINITY) ? 0.f : ex2(c - C)));
   }
-  return resid_val(t, d, st.ct, st.cd, st.invSt, st.invSd, st.mode);
 }
 
-constexpr int kScrFloats = 1024;  // 4 KB: the masses, or one piece's two slices
-
-template <int BF16>
-__device__ void final_select(const DenseParams& P, int b, int lane, float* scr) {
-  const int G = P.G, V = P.V, np = P.g.np, pe = P.g.pe;
-  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
-  const bool staged = np <= kScrFloats;
-  // the mass copies and the stop-record load are in flight together
-  if (staged)
-    for (int k = lane * 4; k < np; k += 128) cp_async16(scr + k, rm + k);
-  StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
-  const float us = P.u_s[b];
-  const int n = st.n;
-  ff T{0.f, 0.f};
-  cp_async_wait_all();
-  __syncwarp();
-  if (st.mode != 2) {
-    const unsigned char* trow = target_row(P, b, n);
-    const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, n) : nullptr;
-    const float* mv = staged ? scr : rm;
-    const int per = (np + 31) / 32;
-    const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
-    ff ls{0.f, 0.f};
-    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, staged ? mv[k] : __ldcg(mv + k));
-    ff ex = warp_exclusive_scan_ff(ls, lane);
-    T = ff_shfl(ff_add(ex, ls), 31);
-    if (!(T.hi > 0.f) && st.mode == 0) {
-      // zero residual after a rejection (only through rounding): draw from p_n
-      st.mode = 1;
-      drow = nullptr;
-      for (int k = 0; k < np; ++k) {
-        const int y0 = k * pe, ne = min(pe, V - y0);
-        float sum = 0.f;
-        for (int e = lane; e < ne; e += 32)
-          sum += resid_val(load_logit(trow, y0 + e, BF16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
-        sum = warp_sum(sum);
-        if (lane == 0) {
-          if (staged)
-            scr[k] = sum;
-          else
-            rm[k] = sum;
-        }
-      }
-      __threadfence();
-      __syncwarp();
-      ls = ff{0.f, 0.f};
-      for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, staged ? scr[k] : __ldcg(rm + k));
-      ex = warp_exclusive_scan_ff(ls, lane);
-      T = ff_shfl(ff_add(ex, ls), 31);
+// reduce piece `it` held in rt / rd into the warp's segment accumulator
+__device__ __forceinline__ void piece_accumulate(const DenseParams& P, const Item& it,
+                                                 const uint4 (&rt)[4], const uint4 (&rd)[4],
+                                                 int lane, SegAcc& a) {
+  const int pe = P.g.pe;
+  const bool has_d = it.j < P.G;
+  float ct, st;
+  piece_stats(rt, P.bf16, ct, st);
+  fold(ct, st, a.Ct, a.St);
+  if (has_d) {
+    float cd, sd;
+    piece_stats(rd, P.bf16, cd, sd);
+    fold(cd, sd, a.Cd, a.Sd);
+    const int ne = min(pe, P.V - it.k * pe);
+    const int xl = __ldg(P.x + (size_t)it.b * P.G + it.j) - it.k * pe;
+    if (xl >= 0 && xl < ne) {
+      a.tb = piece_element(rt, xl, P.bf16, lane);
+      a.db = piece_element(rd, xl, P.bf16, lane);
     }
-    const ff target = ff_mul_f(T, us);
-    // piece level
-    const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && ff_gt(ff_add(ex, ls), target));
-    int kstar = -1;
-    ff base{0.f, 0.f};
-    bool clamp = false;
-    if (hit) {
-      const int fl = __ffs(hit) - 1;
-      if (lane == fl) {
-        ff acc = ex;
-        ff prev = ex;
-        for (int k = k0; k < k1; ++k) {
-          prev = acc;
-          acc = ff_add_f(acc, staged ? scr[k] : __ldcg(rm + k));
-          if (ff_gt(acc, target)) {
-            kstar = k;
-            base = prev;
-            break;
-          }
-        }
-        if (kstar < 0) {  // rounding between the two sums: last piece of the lane
-          kstar = k1 - 1;
-          base = prev;
-        }
-      }
-      kstar = __shfl_sync(0xffffffffu, kstar, fl);
-      base = ff_shfl(base, fl);
-    } else {
-      clamp = true;  // u*T at or past the total: last piece with mass
-      int last = -1;
-      for (int k = k0; k < k1; ++k)
-        if ((staged ? scr[k] : __ldcg(rm + k)) > 0.f) last = k;
-      for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-      kstar = last < 0 ? 0 : last;
-    }
-    __syncwarp();
-    // element level within piece kstar: stage its target and draft slices
-    const int y0 = kstar * pe, ne = min(pe, V - y0);
-    const float* tsm = scr;
-    const float* dsm = scr + 512;  // 2 KB in
-    if (P.aligned) {
-      const int nchunk = (ne * (BF16 ? 2 : 4)) / 16;  // whole 16-byte chunks (rows are aligned)
-      const unsigned char* ts = trow + (size_t)y0 * (BF16 ? 2 : 4);
-      const unsigned char* ds = drow ? drow + (size_t)y0 * (BF16 ? 2 : 4) : nullptr;
-      for (int c = lane; c < nchunk; c += 32) {
-        cp_async16(reinterpret_cast<unsigned char*>(scr) + 16 * c, ts + 16 * c);
-        if (ds) cp_async16(reinterpret_cast<unsigned char*>(scr + 512) + 16 * c, ds + 16 * c);
-      }
-      cp_async_wait_all();
-    } else {
-      for (int e = lane; e < ne; e += 32) {
-        if (BF16) {
-          reinterpret_cast<uint16_t*>(scr)[e] = reinterpret_cast<const uint16_t*>(trow)[y0 + e];
-          if (drow) reinterpret_cast<uint16_t*>(scr + 512)[e] = reinterpret_cast<const uint16_t*>(drow)[y0 + e];
-        } else {
-          scr[e] = reinterpret_cast<const float*>(trow)[y0 + e];
-          if (drow) scr[512 + e] = reinterpret_cast<const float*>(drow)[y0 + e];
-        }
-      }
-    }
-    if (!drow) {  // bonus / fallback: the draft slice is unused; keep it finite
-      for (int e = lane; e < 512; e += 32) scr[512 + e] = 0.f;
-    }
-    __syncwarp();
-    const int q = (ne + 31) / 32;
-    const int e0 = min(ne, lane * q), e1 = min(ne, e0 + q);
-    ff es{0.f, 0.f};
-    int lastpos = -1;
-    for (int e = e0; e < e1; ++e) {
-      const float rv = piece_val<BF16>(tsm, dsm, e, st);
-      es = ff_add_f(es, rv);
-      if (rv > 0.f) lastpos = e;
-    }
-    const ff eex = warp_exclusive_scan_ff(es, lane);
-    const ff tl = ff_sub(target, base);
-    const unsigned ehit =
-        clamp ? 0u : __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(eex, es), tl));
-    int y;
-    if (ehit) {
-      const int fl = __ffs(ehit) - 1;
-      int yy = -1;
-      if (lane == fl) {
-        ff acc = ff_add(base, eex);
-        for (int e = e0; e < e1; ++e) {
-          acc = ff_add_f(acc, piece_val<BF16>(tsm, dsm, e, st));
-          if (ff_gt(acc, target)) {
-            yy = e;
-            break;
-          }
-        }
-        if (yy < 0) yy = lastpos >= 0 ? lastpos : e1 - 1;
-      }
-      y = y0 + __shfl_sync(0xffffffffu, yy, fl);
-    } else {
-      int lp = lastpos;
-      for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
-      y = y0 + (lp < 0 ? 0 : lp);
-    }
-    if (lane == 0) P.tok_out[(size_t)b * (G + 1) + n] = y;
   }
-  // the masses are consumed: leave the workspace zero
-  for (int k = lane; k < np; k += 32) rm[k] = 0.f;
-  if (lane == 0) {
-    StopInfo* sp = ws_at<StopInfo>(P, P.L.stop) + b;
-    if (P.keep_stop) {  // read (and cleared) by the residual-output kernel
-      sp->mode = st.mode;
-      sp->T = (double)T.hi + (double)T.lo;
-    } else {
-      zero32(sp);
-    }
-    ws_at<uint32_t>(P, P.L.cnt_res)[b] = 0;
-  }
-  __syncwarp();
 }
 
-// ---------------------------------------------------------------------------
-// kernel 2: residual (or p) masses of one 32 KB chunk of the stop position's
-// rows, one per piece; the CTA completing a row draws its token
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 2) dense_resid_kernel(const __grid_constant__ DenseParams P) {
-  __shared__ __align__(16) float scr[kScrFloats];
-  __shared__ int s_last;
+__global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const __grid_constant__ DenseParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nc = P.g.nc, pe = P.g.pe;
-  const int b = (int)(blockIdx.x / nc);
-  const int c = (int)(blockIdx.x - (long long)b * nc);
-  const int k = c * kWarps + warp;
-  const StopInfo st = ldcg32(ws_at<StopInfo>(P, P.L.stop) + b);
-  if (k < P.g.np) {
-    float mass = 0.f;
-    if (st.mode != 2) {
+  const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
+  const long long W = (long long)P.B * (G + 1) * np;
+  const long long nwt = (long long)gridDim.x * kWarps;
+  const long long gw = (long long)blockIdx.x * kWarps + warp;
+  const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
+  // the dependent row kernel may be scheduled as soon as SMs free up; it waits
+  // for this whole grid (and its memory) before it reads anything
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (lo >= hi) return;
+  const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
+
+  if (!P.aligned) {  // rows not 16-byte aligned: plain loads, no ring
+    Item it = item_at(lo, G, np);
+    SegAcc acc;
+    seg_begin(acc, it, lo);
+    for (long long w = lo; w < hi; ++w, item_next(it, G, np)) {
+      if (it.b != acc.b || it.j != acc.j) {
+        seg_write(P, acc, lane);
+        seg_begin(acc, it, w);
+      }
+      const int ne = min(pe, P.V - it.k * pe);
+      const size_t off = (size_t)it.k * kPieceBytes;
+      uint4 rt[4], rd[4];
+      load_piece(target_row(P, it.b, it.j) + off, ne, P.bf16, 0, lane, rt);
+      if (it.j < G)
+        load_piece(draft_row(P, it.b, it.j) + off, ne, P.bf16, 0, lane, rd);
+      else
+        for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
+      piece_accumulate(P, it, rt, rd, lane, acc);
+    }
+    seg_write(P, acc, lane);
+    return;
+  }
+
+  unsigned char* ring = smem_raw + (size_t)warp * kStages * kStageBytes;
+  Item in = item_at(lo, G, np), out = in;
+  long long wi = lo;
+#pragma unroll
+  for (int s = 0; s < kStages - 1; ++s) {
+    if (wi < hi) {
+      issue_item(P, in, ring + s * kStageBytes, lane);
+      item_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+  }
+  int slot = 0, islot = kStages - 1;
+  SegAcc acc;
+  seg_begin(acc, out, lo);
+  for (long long w = lo; w < hi; ++w) {
+    if (out.b != acc.b || out.j != acc.j) {
+      seg_write(P, acc, lane);
+      seg_begin(acc, out, w);
+    }
+    if (wi < hi) {
+      issue_item(P, in, ring + islot * kStageBytes, lane);
+      item_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+    cp_async_wait_group<kStages - 1>();
+    const unsigned char* stage = ring + slot * kStageBytes;
+    const int ne = min(pe, P.V - out.k * pe);
+    const bool has_d = out.j < G;
+    uint4 rt[4], rd[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      const bool v = vi * epv < ne;
+      rt[i] = v ? *reinterpret_cast<const uint4*>(stage + 16 * vi) : make_uint4(ninf, ninf, ninf, ninf);
+      rd[i] = (v && has_d) ? *reinterpret_cast<const uint4*>(stage + kPieceBytes + 16 * vi)
+                           : make_uint4(ninf, ninf, ninf, ninf);
+    }
+    piece_accumulate(P, out, rt, rd, lane, acc);
+    item_next(out, G, np);
+    slot = (slot + 1 == kStages) ? 0 : slot + 1;
+    islot = (islot + 1 == kStages) ? 0 : islot + 1;
+  }
+  seg_write(P, acc, lane);
+  cp_async_wait_group<0>();
+}
+
+// ---------------------------------------------------------------------------
+// kernel 2: everything after the statistics, one thread-block cluster of C
+// CTAs per row.  Every CTA of the cluster finalises the row from the piece
+// records (the same arithmetic, so the same n and constants), then computes
+// the residual (or p) mass of its share of the stop position's pieces.  After
+// a cluster barrier the rank-0 CTA draws the token: a prefix over the row's
+// piece masses picks the piece, a prefix over that piece's element values
+// picks the token.  Both prefixes are block-wide scans in fp64 (a few hundred
+// additions per row), so no thread walks more than a handful of values.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ unsigned cluster_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// all threads of every CTA of the cluster; orders their earlier memory
+// operations before everything after the barrier, cluster-wide
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float logit_at(const unsigned char* row, int y, int bf16) {
+  return bf16 ? bf16_to_f32(__ldg(reinterpret_cast<const uint16_t*>(row) + y))
+              : __ldg(reinterpret_cast<const float*>(row) + y);
+}
+
+struct SelShared {
+  float whi[kWarps], wlo[kWarps];
+  ff base;
+  int wa[kWarps], wb[kWarps];
+  int kstar, y;
+};
+
+// Block-wide exclusive prefix of v in float-float; `total` receives the sum.
+// (float-float rather than fp64: GB300 runs fp64 at a small fraction of the
+// fp32 rate, and here every thread of the block takes part.)
+__device__ __forceinline__ ff block_exclusive_scan_ff(ff v, SelShared& S, ff& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  ff x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const ff y = ff_shfl_up(x, o);
+    if (lane >= o) x = ff_add(x, y);
+  }
+  ff ex = ff_shfl_up(x, 1);
+  if (lane == 0) ex = ff{0.f, 0.f};
+  if (lane == 31) {
+    S.whi[warp] = x.hi;
+    S.wlo[warp] = x.lo;
+  }
+  __syncthreads();
+  ff wbase{0.f, 0.f}, tot{0.f, 0.f};
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    const ff t{S.whi[w], S.wlo[w]};
+    if (w < warp) wbase = ff_add(wbase, t);
+    tot = ff_add(tot, t);
+  }
+  __syncthreads();  // whi / wlo may be reused
+  total = tot;
+  return ff_add(wbase, ex);
+}
+
+// block-wide: the first thread with `cond` (kThreads if none) and the largest
+// `v` (one ballot / reduction per warp, then one pass over the warps; no
+// contended shared-memory atomics)
+__device__ __forceinline__ void block_first_and_max(bool cond, int v, SelShared& S, int& first,
+                                                    int& vmax) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, cond);
+  const int wm = (int)__reduce_max_sync(0xffffffffu, (unsigned)(v + 1)) - 1;  // v >= -1
+  if (lane == 0) {
+    S.wa[warp] = bal ? warp * 32 + __ffs(bal) - 1 : kThreads;
+    S.wb[warp] = wm;
+  }
+  __syncthreads();
+  int f = kThreads, m = -1;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    f = min(f, S.wa[w]);
+    m = max(m, S.wb[w]);
+  }
+  __syncthreads();  // wa / wb may be reused
+  first = f;
+  vmax = m;
+}
+
+// the token of row b from its piece masses (whole CTA); returns T
+__device__ double select_row(const DenseParams& P, int b, StopInfo& st, SelShared& S) {
+  const int t = threadIdx.x;
+  const int V = P.V, np = P.g.np, pe = P.g.pe;
+  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
+  const float us = P.u_s[b];
+  const unsigned char* trow = target_row(P, b, st.n);
+  const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
+  // piece level: thread t sums its run of masses
+  const int per = (np + kThreads - 1) / kThreads;
+  const int k0 = min(np, t * per), k1 = min(np, k0 + per);
+  ff ls{0.f, 0.f};
+  for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, __ldcg(rm + k));
+  ff T;
+  ff ex = block_exclusive_scan_ff(ls, S, T);
+  if (!(T.hi > 0.f) && st.mode == 0) {
+    // zero residual after a rejection (only through rounding): draw from p_n
+    st.mode = 1;
+    drow = nullptr;
+    const int warp = t >> 5, lane = t & 31;
+    for (int k = warp; k < np; k += kWarps) {
+      const int y0 = k * pe, ne = min(pe, V - y0);
+      float sum = 0.f;
+      for (int e = lane; e < ne; e += 32)
+        sum += resid_val(logit_at(trow, y0 + e, P.bf16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
+      sum = warp_sum(sum);
+      if (lane == 0) rm[k] = sum;
+    }
+    __syncthreads();
+    ls = ff{0.f, 0.f};
+    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, __ldcg(rm + k));
+    ex = block_exclusive_scan_ff(ls, S, T);
+  }
+  const ff target = ff_mul_f(T, us);
+  int lastk = -1;
+  for (int k = k0; k < k1; ++k)
+    if (__ldcg(rm + k) > 0.f) lastk = k;
+  int cross, klast;
+  block_first_and_max(k1 > k0 && ff_gt(ff_add(ex, ls), target), lastk, S, cross, klast);
+  if (t == cross) {  // the first piece whose inclusive prefix exceeds the target
+    ff acc = ex, base = ex;
+    int ks = k0;
+    for (int k = k0; k < k1; ++k) {
+      base = acc;
+      acc = ff_add_f(acc, __ldcg(rm + k));
+      ks = k;
+      if (ff_gt(acc, target)) break;
+    }
+    S.kstar = ks;
+    S.base = base;
+  } else if (t == 0 && cross == kThreads) {  // u*T at or past the total: last piece with mass
+    S.kstar = max(klast, 0);
+    S.base = ff{0.f, 0.f};
+  }
+  __syncthreads();
+  const bool clamp = cross == kThreads;
+  const int kstar = S.kstar;
+  const ff base = S.base;
+  // element level: thread t takes the contiguous run [t q, t q + q) of piece kstar
+  constexpr int kMaxQ = kPieceBytes / 2 / kThreads;  // 2 (bf16); fp32 uses 1
+  const int q = pe / kThreads;
+  const int y0 = kstar * pe, ne = min(pe, V - y0);
+  float rv[kMaxQ];
+  float tot = 0.f;
+  int lastpos = -1;
+#pragma unroll
+  for (int i = 0; i < kMaxQ; ++i) {
+    const int e = t * q + i;
+    float r = 0.f;
+    if (i < q && e < ne)
+      r = resid_val(logit_at(trow, y0 + e, P.bf16), drow ? logit_at(drow, y0 + e, P.bf16) : 0.f,
+                    st.ct, st.cd, st.invSt, st.invSd, st.mode);
+    rv[i] = r;
+    tot = __fadd_rn(tot, r);
+    if (r > 0.f) lastpos = e;
+  }
+  ff ptot;
+  const ff lbase = ff_add(base, block_exclusive_scan_ff(ff{tot, 0.f}, S, ptot));
+  int ecross, elast;
+  block_first_and_max(!clamp && ff_gt(ff_add_f(lbase, tot), target), lastpos, S, ecross, elast);
+  if (t == ecross) {
+    ff acc = lbase;
+    int yy = -1, lp = -1;
+#pragma unroll
+    for (int i = 0; i < kMaxQ; ++i) {
+      if (i < q && yy < 0) {
+        acc = ff_add_f(acc, rv[i]);
+        if (rv[i] > 0.f) lp = t * q + i;
+        if (ff_gt(acc, target)) yy = t * q + i;
+      }
+    }
+    // rounding between the two sums: the run's last element with mass
+    if (yy < 0) yy = lp >= 0 ? lp : lastpos;
+    S.y = yy < 0 ? 0 : yy;
+  } else if (t == 0 && ecross == kThreads) {
+    S.y = max(elast, 0);
+  }
+  __syncthreads();
+  if (t == 0) P.tok_out[(size_t)b * (P.G + 1) + st.n] = y0 + S.y;
+  return (double)T.hi + (double)T.lo;
+}
+
+__global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_constant__ DenseParams P) {
+  __shared__ FinShared F;
+  __shared__ SelShared S;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = (int)cluster_size(), r = (int)cluster_rank();
+  const int b = blockIdx.x / C;
+  const bool owner = r == 0;
+  const int G = P.G, np = P.g.np, pe = P.g.pe;
+  // launched as a programmatic dependent of the statistics kernel: wait for
+  // it to complete (and its records to be visible) before reading them
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  finalize_row(P, b, warp, lane, F, owner);
+  StopInfo st = F.st;
+  // residual (or p) masses of this CTA's share of the stop position's pieces
+  if (st.mode != 2) {
+    const int k_lo = (int)((long long)r * np / C), k_hi = (int)((long long)(r + 1) * np / C);
+    const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
+    for (int k = k_lo + warp; k < k_hi; k += kWarps) {
       const int ne = min(pe, P.V - k * pe);
       const size_t off = (size_t)k * kPieceBytes;
       uint4 rt[4], rd[4];
       load_piece(target_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rt);
-      if (st.mode == 0) {
+      if (st.mode == 0)
         load_piece(draft_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rd);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) rd[i] = rt[i];  // unused by mode 1
-      }
-      mass = piece_resid(rt, rd, P.bf16, st);
+      else
+        for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
+      const float mass = piece_resid(rt, rd, P.bf16, st);
+      if (lane == 0) ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
     }
-    if (lane == 0) ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned old = atomicAdd(ws_at<uint32_t>(P, P.L.cnt_res) + b, 1u);
-    s_last = (old == (unsigned)nc - 1);
+  cluster_barrier();  // every CTA's masses are written; every record was read
+  if (!owner) return;
+  double T = 0.0;
+  if (st.mode != 2) T = select_row(P, b, st, S);
+  // the records, the masses and the stop record are consumed: leave the workspace zero
+  UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * np;
+  for (int i = threadIdx.x; i < (G + 1) * np; i += kThreads) zero32(up_row + i);
+  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
+  for (int k = threadIdx.x; k < np; k += kThreads) rm[k] = 0.f;
+  if (threadIdx.x == 0 && P.keep_stop) {  // read (and cleared) by the residual-output kernel
+    st.T = T;
+    ws_at<StopInfo>(P, P.L.stop)[b] = st;
   }
-  __syncthreads();
-  if (!s_last || warp != 0) return;
-  __threadfence();  // every chunk's masses are visible before they are read
-  if (P.bf16)
-    final_select<1>(P, b, lane, scr);
-  else
-    final_select<0>(P, b, lane, scr);
 }
 
 // residual_out: the distribution the emitted token was drawn from.  One CTA
@@ -715,13 +866,45 @@ __global__ void dense_resid_out_kernel(const __grid_constant__ DenseParams P, fl
 }  // namespace
 
 cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
-  const long long g1 = (long long)p.B * (p.G + 1) * p.g.nc;
-  const long long g2 = (long long)p.B * p.g.nc;
-  dense_stats_kernel<<<(unsigned)g1, kThreads, 0, s>>>(p);
-  cudaError_t e = cudaGetLastError();
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  dense_resid_kernel<<<(unsigned)g2, kThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {  // once per device: SM count and the ring's shared memory
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dense_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kStatsSmem);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n;
+  }
+  const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
+  long long grid = sms[dev];
+  if (grid * kWarps > pieces) grid = (pieces + kWarps - 1) / kWarps;
+  dense_stats_kernel<<<(unsigned)grid, kThreads, kStatsSmem, s>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // clusters of C CTAs per row: about two CTAs per SM in all, at most 8
+  int C = (int)((2ll * sms[dev]) / p.B);
+  C = C < 1 ? 1 : (C > 8 ? 8 : C);
+  if (C > p.g.np) C = p.g.np;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((long long)p.B * C), 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, dense_row_kernel, p);
 }
 
 cudaError_t launch_dense_resid_out(const DenseParams& p, float* resid_out, cudaStream_t s) {

@@ -45,10 +45,10 @@ inline DenseGeom dense_geom(int V, int es) {
   return g;
 }
 
-// Combined statistics of one chunk of a (row, position): S = sum 2^(v*log2e - c)
-// over the chunk's elements, c = log2e * (max logit); tx / dx are the target
-// and draft logits at the draft token when the chunk holds it (kNoTokenBits
-// otherwise).
+// Statistics of one piece of a (row, position): S = sum 2^(v*log2e - c) over
+// the piece's elements, c = log2e * (max logit), target and draft; tx / dx are
+// the target and draft logits at the draft token when the piece holds it
+// (kNoTokenBits otherwise).
 struct UnitPart {
   float St_hi, St_lo, Sd_hi, Sd_lo;  // float-float sums
   float ct, cd;
@@ -71,7 +71,7 @@ struct StopInfo {
 };
 
 struct DenseLayout {  // byte offsets into the workspace
-  size_t cnt_row, cnt_res, upart, stop, rmass, total;
+  size_t upart, stop, rmass, total;
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -79,12 +79,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline DenseLayout dense_layout(long long B, int G, const DenseGeom& g) {
   DenseLayout L;
   size_t o = sizeof(WsHeader);
-  L.cnt_row = o;
-  o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
-  L.cnt_res = o;
-  o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
   L.upart = o;
-  o = align_up(o + sizeof(UnitPart) * (size_t)B * (size_t)(G + 1) * (size_t)g.nc, 256);
+  o = align_up(o + sizeof(UnitPart) * (size_t)B * (size_t)(G + 1) * (size_t)g.np, 256);
   L.stop = o;
   o = align_up(o + sizeof(StopInfo) * (size_t)B, 256);
   L.rmass = o;
