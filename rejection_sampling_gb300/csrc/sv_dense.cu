@@ -270,6 +270,8 @@ __device__ __forceinline__ void warp_combine(float& C, ff& S) {
 
 struct FinShared {
   float c[4][kMaxG];  // per position: Ct, St, Cd, Sd (the stop position's constants)
+  float u[kMaxG];     // u_accept of the row (prefetched)
+  int x[kMaxG];       // draft tokens of the row (prefetched)
   int n;              // first rejected position (G + 1: none)
   int err;
   StopInfo st;        // the result: stop position and its draw constants
@@ -281,8 +283,11 @@ struct FinShared {
 // every token but token n.
 __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, FinShared& F,
                              bool owner) {
-  const int G = P.G, nc = P.g.np;  // one record per piece
-  UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * nc;
+  const int G = P.G, np = P.g.np;
+  const UnitPart* rec = ws_at<UnitPart>(P, P.L.upart);
+  // the statistics grid gave warp g the pieces [lo(g), lo(g + 1)), lo(g) =
+  // g W / nwt; a segment record sits at the first piece of the segment
+  const long long W = (long long)P.B * (G + 1) * np, nwt = P.stats_warps;
   if (threadIdx.x == 0) {
     F.n = G + 1;
     F.err = 0;
@@ -292,24 +297,17 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     float Ct = -INFINITY, Cd = -INFINITY;
     ff St{0.f, 0.f}, Sd{0.f, 0.f};
     uint32_t txb = kNoTokenBits, dxb = kNoTokenBits;
-    for (int k0 = 0; k0 < nc; k0 += 4 * 32) {
-      // four records per lane in flight at once, then zeroed, then combined
-      UnitPart u[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int k = k0 + lane + 32 * q;
-        if (k < nc) u[q] = ldcg32(up_row + (size_t)j * nc + k);
-      }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int k = k0 + lane + 32 * q;
-        if (k < nc && !(u[q].St_hi == 0.f && u[q].ct == 0.f)) {  // empty slots hold zeros
-          combine_part(u[q], Ct, St, Cd, Sd);
-          if (__float_as_uint(u[q].tx) != kNoTokenBits) {
-            txb = __float_as_uint(u[q].tx);
-            dxb = __float_as_uint(u[q].dx);
-          }
-        }
+    const long long P0 = ((long long)b * (G + 1) + j) * np, P1 = P0 + np;
+    // warps whose ranges meet [P0, P1): lo(g) <= P0 for the first, lo(g) < P1 for the last
+    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    for (long long g = g0 + lane; g <= g1; g += 32) {
+      const long long lo = g * W / nwt, lo1 = (g + 1) * W / nwt;
+      if (lo1 <= lo) continue;  // an empty range writes nothing
+      const UnitPart u = ldcg32(rec + (lo > P0 ? lo : P0));
+      combine_part(u, Ct, St, Cd, Sd);
+      if (__float_as_uint(u.tx) != kNoTokenBits) {
+        txb = __float_as_uint(u.tx);
+        dxb = __float_as_uint(u.dx);
       }
     }
     warp_combine(Ct, St);
@@ -338,7 +336,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
         ratio = exp2f(ff_to_f(ff_sub(ea, ed))) * __fdiv_rn(Sdf, Stf);
       }
       a = fminf(ratio, 1.f);
-      acc = P.u_acc[(size_t)b * G + j] < a;
+      acc = F.u[j] < a;
     }
     if (lane == 0) {
       if (owner && j < G && P.acc_out)
@@ -386,7 +384,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     if (err)
       tok[j] = -1;
     else if (j < n)
-      tok[j] = P.x[(size_t)b * G + j];
+      tok[j] = F.x[j];
     else if (j > n)
       tok[j] = -1;
   }
@@ -401,9 +399,12 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
 // Each lane copies, and later reads, only its own vectors, so the ring needs
 // no synchronisation beyond the lane's own cp.async groups.
 // ---------------------------------------------------------------------------
-constexpr int kStages = 3;
+constexpr int kStatsWarps = 24;  // warps per statistics CTA
+constexpr int kStatsCtas = 1;    // statistics CTAs per SM
+constexpr int kStatsThreads = 32 * kStatsWarps;
+constexpr int kStages = 2;
 constexpr int kStageBytes = 2 * kPieceBytes;
-constexpr size_t kStatsSmem = (size_t)kWarps * kStages * kStageBytes;
+constexpr size_t kStatsSmem = (size_t)kStatsWarps * kStages * kStageBytes;
 
 struct Item {  // piece k of row-position (b, j)
   int b, j, k;
@@ -516,13 +517,13 @@ __device__ __forceinline__ void piece_accumulate(const DenseParams& P, const Ite
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1) dense_stats_kernel(const __grid_constant__ DenseParams P) {
+__global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
   const long long W = (long long)P.B * (G + 1) * np;
-  const long long nwt = (long long)gridDim.x * kWarps;
-  const long long gw = (long long)blockIdx.x * kWarps + warp;
+  const long long nwt = (long long)gridDim.x * kStatsWarps;
+  const long long gw = (long long)blockIdx.x * kStatsWarps + warp;
   const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
   // the dependent row kernel may be scheduled as soon as SMs free up; it waits
   // for this whole grid (and its memory) before it reads anything
@@ -634,7 +635,8 @@ __device__ __forceinline__ float logit_at(const unsigned char* row, int y, int b
 
 struct SelShared {
   float whi[kWarps], wlo[kWarps];
-  ff base;
+  ff base, T;
+  int clamp;
   int wa[kWarps], wb[kWarps];
   int kstar, y;
 };
@@ -669,6 +671,17 @@ __device__ __forceinline__ ff block_exclusive_scan_ff(ff v, SelShared& S, ff& to
   return ff_add(wbase, ex);
 }
 
+// shared-memory address of `p` in the rank-0 CTA of the cluster, and a store there
+__device__ __forceinline__ uint32_t map_rank0(const void* p) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(smem_u32(p)));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+constexpr int kMassSmem = 2048;  // pieces per row whose masses are kept on chip
+
 // block-wide: the first thread with `cond` (kThreads if none) and the largest
 // `v` (one ballot / reduction per warp, then one pass over the warps; no
 // contended shared-memory atomics)
@@ -693,62 +706,78 @@ __device__ __forceinline__ void block_first_and_max(bool cond, int v, SelShared&
   vmax = m;
 }
 
-// the token of row b from its piece masses (whole CTA); returns T
-__device__ double select_row(const DenseParams& P, int b, StopInfo& st, SelShared& S) {
-  const int t = threadIdx.x;
+// the token of row b from its piece masses `mv` (shared memory of this CTA,
+// or the workspace); whole CTA; returns T
+__device__ double select_row(const DenseParams& P, int b, StopInfo& st, float* mv, bool mv_shared,
+                             SelShared& S) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  // masses written by other CTAs: shared memory, or global memory read around L1
+  auto mass = [&](int k) -> float { return mv_shared ? mv[k] : __ldcg(mv + k); };
   const int V = P.V, np = P.g.np, pe = P.g.pe;
-  float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
   const float us = P.u_s[b];
   const unsigned char* trow = target_row(P, b, st.n);
   const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
-  // piece level: thread t sums its run of masses
-  const int per = (np + kThreads - 1) / kThreads;
-  const int k0 = min(np, t * per), k1 = min(np, k0 + per);
-  ff ls{0.f, 0.f};
-  for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, __ldcg(rm + k));
-  ff T;
-  ff ex = block_exclusive_scan_ff(ls, S, T);
-  if (!(T.hi > 0.f) && st.mode == 0) {
+  // piece level, one warp: lane l sums its run of masses, a warp prefix
+  // finds the first piece whose inclusive prefix exceeds u * T
+  const int per = (np + 31) / 32;
+  const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
+  ff T{0.f, 0.f};
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    if (warp == 0) {
+      ff ls{0.f, 0.f};
+      for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, mass(k));
+      const ff ex = warp_exclusive_scan_ff(ls, lane);
+      const ff tot = ff_shfl(ff_add(ex, ls), 31);
+      const ff target = ff_mul_f(tot, us);
+      const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && ff_gt(ff_add(ex, ls), target));
+      int kstar = 0;
+      ff base{0.f, 0.f};
+      if (hit) {
+        const int fl = __ffs(hit) - 1;
+        if (lane == fl) {
+          ff acc = ex;
+          for (int k = k0; k < k1; ++k) {
+            base = acc;
+            acc = ff_add_f(acc, mass(k));
+            kstar = k;
+            if (ff_gt(acc, target)) break;
+          }
+        }
+        kstar = __shfl_sync(0xffffffffu, kstar, fl);
+        base = ff_shfl(base, fl);
+      } else {  // u*T at or past the total: the last piece with mass
+        int last = -1;
+        for (int k = k0; k < k1; ++k)
+          if (mass(k) > 0.f) last = k;
+        last = (int)__reduce_max_sync(0xffffffffu, (unsigned)(last + 1)) - 1;
+        kstar = last < 0 ? 0 : last;
+      }
+      if (lane == 0) {
+        S.kstar = kstar;
+        S.base = base;
+        S.T = tot;
+        S.clamp = hit == 0u;
+      }
+    }
+    __syncthreads();
+    T = S.T;
+    if (T.hi > 0.f || st.mode != 0 || attempt == 1) break;
     // zero residual after a rejection (only through rounding): draw from p_n
     st.mode = 1;
     drow = nullptr;
-    const int warp = t >> 5, lane = t & 31;
     for (int k = warp; k < np; k += kWarps) {
       const int y0 = k * pe, ne = min(pe, V - y0);
       float sum = 0.f;
       for (int e = lane; e < ne; e += 32)
         sum += resid_val(logit_at(trow, y0 + e, P.bf16), 0.f, st.ct, st.cd, st.invSt, st.invSd, 1);
       sum = warp_sum(sum);
-      if (lane == 0) rm[k] = sum;
+      if (lane == 0) mv[k] = sum;
     }
+    __threadfence_block();
     __syncthreads();
-    ls = ff{0.f, 0.f};
-    for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, __ldcg(rm + k));
-    ex = block_exclusive_scan_ff(ls, S, T);
   }
   const ff target = ff_mul_f(T, us);
-  int lastk = -1;
-  for (int k = k0; k < k1; ++k)
-    if (__ldcg(rm + k) > 0.f) lastk = k;
-  int cross, klast;
-  block_first_and_max(k1 > k0 && ff_gt(ff_add(ex, ls), target), lastk, S, cross, klast);
-  if (t == cross) {  // the first piece whose inclusive prefix exceeds the target
-    ff acc = ex, base = ex;
-    int ks = k0;
-    for (int k = k0; k < k1; ++k) {
-      base = acc;
-      acc = ff_add_f(acc, __ldcg(rm + k));
-      ks = k;
-      if (ff_gt(acc, target)) break;
-    }
-    S.kstar = ks;
-    S.base = base;
-  } else if (t == 0 && cross == kThreads) {  // u*T at or past the total: last piece with mass
-    S.kstar = max(klast, 0);
-    S.base = ff{0.f, 0.f};
-  }
-  __syncthreads();
-  const bool clamp = cross == kThreads;
+  const bool clamp = S.clamp;
   const int kstar = S.kstar;
   const ff base = S.base;
   // element level: thread t takes the contiguous run [t q, t q + q) of piece kstar
@@ -798,13 +827,20 @@ __device__ double select_row(const DenseParams& P, int b, StopInfo& st, SelShare
 __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_constant__ DenseParams P) {
   __shared__ FinShared F;
   __shared__ SelShared S;
+  __shared__ float s_mass[kMassSmem];  // the row's piece masses (rank 0), when they fit
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = (int)cluster_size(), r = (int)cluster_rank();
+  const bool in_smem = P.g.np <= kMassSmem;
   const int b = blockIdx.x / C;
   const bool owner = r == 0;
   const int G = P.G, np = P.g.np, pe = P.g.pe;
-  // launched as a programmatic dependent of the statistics kernel: wait for
-  // it to complete (and its records to be visible) before reading them
+  // inputs first (they do not come from the statistics kernel) ...
+  for (int j = threadIdx.x; j < G; j += kThreads) {
+    F.u[j] = P.u_acc[(size_t)b * G + j];
+    F.x[j] = P.x[(size_t)b * G + j];
+  }
+  // ... then, launched as a programmatic dependent of the statistics kernel,
+  // wait for it to complete (and its records to be visible)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   finalize_row(P, b, warp, lane, F, owner);
   StopInfo st = F.st;
@@ -822,13 +858,20 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
       else
         for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
       const float mass = piece_resid(rt, rd, P.bf16, st);
-      if (lane == 0) ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
+      if (lane == 0) {
+        if (in_smem)  // into the rank-0 CTA's shared memory
+          st_cluster_f32(map_rank0(&s_mass[k]), mass);
+        else
+          ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
+      }
     }
   }
   cluster_barrier();  // every CTA's masses are written; every record was read
   if (!owner) return;
   double T = 0.0;
-  if (st.mode != 2) T = select_row(P, b, st, S);
+  if (st.mode != 2)
+    T = select_row(P, b, st, in_smem ? s_mass : ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4,
+                   in_smem, S);
   // the records, the masses and the stop record are consumed: leave the workspace zero
   UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * np;
   for (int i = threadIdx.x; i < (G + 1) * np; i += kThreads) zero32(up_row + i);
@@ -881,9 +924,11 @@ cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
     sms[dev] = n;
   }
   const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
-  long long grid = sms[dev];
-  if (grid * kWarps > pieces) grid = (pieces + kWarps - 1) / kWarps;
-  dense_stats_kernel<<<(unsigned)grid, kThreads, kStatsSmem, s>>>(p);
+  long long grid = (long long)sms[dev] * kStatsCtas;
+  if (grid * kStatsWarps > pieces) grid = (pieces + kStatsWarps - 1) / kStatsWarps;
+  DenseParams q = p;
+  q.stats_warps = grid * kStatsWarps;
+  dense_stats_kernel<<<(unsigned)grid, kStatsThreads, kStatsSmem, s>>>(q);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // clusters of C CTAs per row: about two CTAs per SM in all, at most 8
@@ -904,7 +949,7 @@ cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, dense_row_kernel, p);
+  return cudaLaunchKernelEx(&cfg, dense_row_kernel, q);
 }
 
 cudaError_t launch_dense_resid_out(const DenseParams& p, float* resid_out, cudaStream_t s) {

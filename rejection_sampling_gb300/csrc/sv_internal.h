@@ -105,6 +105,7 @@ struct DenseParams {
   int bf16;       // 1: bf16 logits, 0: fp32
   int aligned;    // 1: rows 16-byte aligned -> 16-byte vector loads
   int keep_stop;  // 1: residual_out requested; its kernel reads and clears stop[]
+  long long stats_warps;  // warps of the statistics grid (their piece ranges locate the records)
 };
 
 // ---------------------------------------------------------------------------
