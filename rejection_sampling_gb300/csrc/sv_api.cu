@@ -87,6 +87,9 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
     p.anyorder = 0;
     p.bf16 = (dtype == SV_BF16);
     p.vstride = small_vstride(V);
+    p.flat = !p.bf16 && p.vstride == V && ((size_t)(gamma + 1) * V * 4) % 16 == 0 &&
+             ((size_t)gamma * V * 4) % 16 == 0 && aligned_to(target_logits, 16) &&
+             (gamma == 0 || aligned_to(draft_logits, 16));
     return launch_status(sv::launch_small(p, s));
   }
 
@@ -203,6 +206,8 @@ int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv
   p.anyorder = 1;
   p.bf16 = (dtype == SV_BF16);
   p.vstride = small_vstride(V);
+  p.flat = !p.bf16 && p.vstride == V && D == W && ((size_t)D * V * 4) % 16 == 0 &&
+           aligned_to(target_logits, 16) && aligned_to(draft_logits, 16);
   return launch_status(sv::launch_small(p, (cudaStream_t)stream));
 }
 

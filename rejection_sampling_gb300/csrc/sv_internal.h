@@ -130,6 +130,7 @@ struct SmallParams {
   int anyorder;
   int bf16;
   int vstride;  // shared-memory row stride in floats (odd)
+  int flat;     // 1: fp32 row blocks staged whole, in source order, by 16-byte copies
 };
 
 // ---------------------------------------------------------------------------

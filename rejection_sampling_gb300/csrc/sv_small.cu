@@ -78,39 +78,111 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   bad = __any_sync(0xffffffffu, bad);
 
   // ---- stage the rows in shared memory (row r of the warp = position r) ----
-  for (int r = 0; r < R; ++r) {
-    size_t trow, drow;
-    bool hasd;
-    if (P.anyorder) {
-      int s = __shfl_sync(0xffffffffu, sig, r);
-      if (bad) s = 0;
-      trow = drow = (size_t)b * P.D + s;
-      hasd = true;
+  // The R x V block is walked flat, 32 consecutive elements per step, so every
+  // lane works in every step and each row is read contiguously.  fp32 rows
+  // move with 4-byte cp.async (all steps in flight at once); bf16 rows are
+  // widened in registers, kBatch steps of loads in flight before their stores.
+  if (P.flat) {
+    // fp32 blocks whose size and start are 16-byte multiples: copied whole, in
+    // source order (any-order: sequence positions, read through sigma below)
+    const int nt = (P.anyorder ? P.D : NT + 1) * V / 4, nd = (P.anyorder ? P.D : NT) * V / 4;
+    const float4* ts = reinterpret_cast<const float4*>(P.lt) + (size_t)b * nt;
+    const float4* ds = reinterpret_cast<const float4*>(P.ld) + (size_t)b * nd;
+    for (int i = lane; i < nt; i += 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(st + 4 * i)), "l"(ts + i)
+                   : "memory");
+    for (int i = lane; i < nd; i += 32)
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sd + 4 * i)), "l"(ds + i)
+                   : "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else {
+    const int total = R * V;
+    int r = lane / V, y = lane - (lane / V) * V;  // (row, column) of element `lane`
+    auto rows_of = [&](int rr, size_t& trow, size_t& drow, bool& hasd) {
+      if (P.anyorder) {
+        int sg = __shfl_sync(0xffffffffu, sig, rr);
+        if (bad) sg = 0;
+        trow = drow = (size_t)b * P.D + sg;
+        hasd = true;
+      } else {
+        trow = (size_t)b * (NT + 1) + rr;
+        drow = (size_t)b * NT + rr;
+        hasd = rr < NT;
+      }
+    };
+    auto advance = [&]() {  // the next element of this lane, 32 further on
+      y += 32;
+      while (y >= V) {
+        y -= V;
+        ++r;
+      }
+    };
+    if (!P.bf16) {
+      const float* lt = reinterpret_cast<const float*>(P.lt);
+      const float* ld = reinterpret_cast<const float*>(P.ld);
+      for (int base = 0; base < total; base += 32) {
+        const bool on = base + lane < total;
+        const int rr = on ? r : 0;
+        size_t trow, drow;
+        bool hasd;
+        rows_of(rr, trow, drow, hasd);
+        if (on) {
+          asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(st + rr * VS + y)),
+                       "l"(lt + trow * V + y)
+                       : "memory");
+          if (hasd)
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(sd + rr * VS + y)),
+                         "l"(ld + drow * V + y)
+                         : "memory");
+        }
+        advance();
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     } else {
-      trow = (size_t)b * (NT + 1) + r;
-      drow = (size_t)b * NT + r;
-      hasd = r < NT;
-    }
-    for (int y = lane; y < V; y += 32) {
-      st[r * VS + y] = ld_logit(P.lt, trow * V + y, P.bf16);
-      if (hasd) sd[r * VS + y] = ld_logit(P.ld, drow * V + y, P.bf16);
+      constexpr int kBatch = 8;
+      for (int base = 0; base < total; base += 32 * kBatch) {
+        float tv[kBatch], dv[kBatch];
+        int ri[kBatch], yi[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const bool on = base + 32 * q + lane < total;
+          const int rr = on ? r : 0;
+          size_t trow, drow;
+          bool hasd;
+          rows_of(rr, trow, drow, hasd);
+          ri[q] = on ? rr : -1;
+          yi[q] = y;
+          tv[q] = on ? ld_logit(P.lt, trow * V + y, 1) : 0.f;
+          dv[q] = (on && hasd) ? ld_logit(P.ld, drow * V + y, 1) : 0.f;
+          advance();
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          if (ri[q] >= 0) {
+            st[ri[q] * VS + yi[q]] = tv[q];
+            if (P.anyorder || ri[q] < NT) sd[ri[q] * VS + yi[q]] = dv[q];
+          }
+        }
+      }
     }
   }
   __syncwarp();
 
   // ---- per-position statistics and accept test (lane = position) ----
+  // shared-memory row of this lane's position (valid when !bad)
+  const int prow = (P.flat && P.anyorder) ? sig : lane;
   float ct = 0.f, St = 1.f, cd = 0.f, Sd = 1.f, a = 0.f;
   int err = bad, acc = 1, x = 0;
   if (!bad && lane < R) {
-    row_stats(st + lane * VS, V, ct, St);
+    row_stats(st + prow * VS, V, ct, St);
     err |= !stats_ok(ct, St);
     if (lane < NT) {
-      row_stats(sd + lane * VS, V, cd, Sd);
+      row_stats(sd + prow * VS, V, cd, Sd);
       err |= !stats_ok(cd, Sd);
       x = P.anyorder ? P.x[(size_t)b * P.D + sig] : P.x[(size_t)b * NT + lane];
       if (x < 0 || x >= V) err = 1;
       if (!err) {
-        const float tx = st[lane * VS + x], dx = sd[lane * VS + x];
+        const float tx = st[prow * VS + x], dx = sd[prow * VS + x];
         float ratio = 0.f;
         if (tx > -INFINITY && dx > -INFINITY) {
           // log2 p(x) - log2 q(x) formed exactly (two-product), rounded once
@@ -136,7 +208,7 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   int srow = 0;
   if (n >= 0 && (n < NT || !P.anyorder)) {
     mode = (n < NT) ? 0 : 1;
-    srow = n;  // shared-memory row of the stop position
+    srow = (P.flat && P.anyorder) ? __shfl_sync(0xffffffffu, sig, n) : n;  // its shared-memory row
     sct = __shfl_sync(0xffffffffu, ct, n);
     scd = __shfl_sync(0xffffffffu, cd, n);
     sist = 1.f / __shfl_sync(0xffffffffu, St, n);
