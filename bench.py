@@ -426,7 +426,7 @@ def run_ours(args):
                          "median_launch_us": statistics.median(launch_ms) * 1e3},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps,
+            "gpu_launches": 2 * args.steps,  # dense_stats_kernel + dense_row_kernel per call
             "clocks": clocks,
             "variants": variants,
             "kernel_source_sha256_16": kernel_source_hash(),
