@@ -487,6 +487,28 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_calls_only(args):
+    """Profiling driver: the headline workload through spec_verify_dense,
+    args.calls_only times, no timing and no output beyond one status line
+    (ncu's launch filters pick the kernels out)."""
+    import numpy as np
+    import torch
+    import rejection_sampling_gb300 as rs
+    from rejection_sampling_gb300 import workloads as wl
+    rs.build()
+    rs.load()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = wl.make(WORKLOAD, seed=args.seed)
+    t = [to_dev(d[k], dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
+    for _ in range(args.calls_only):
+        rs.spec_verify_dense(*t)
+    torch.cuda.synchronize()
+    rc = rs.check(dev, torch.cuda.current_stream(dev))
+    print(f"{args.calls_only} calls of {WORKLOAD}: {rs.status_string(rc)}")
+    if rc != rs.SV_OK:
+        raise SystemExit(1)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,7 +521,12 @@ def main(argv=None):
     ap.add_argument("--no-e2e", dest="no_e2e", action="store_true")
     ap.add_argument("--no-variants", dest="no_variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
+    ap.add_argument("--calls-only", dest="calls_only", type=int, default=0,
+                    help="profiling driver: N untimed calls on the headline workload")
     args = ap.parse_args(argv)
+    if args.calls_only > 0:
+        run_calls_only(args)
+        return
     if args.impl == "reference":
         args.steps = 5 if args.steps is None else args.steps
         args.warmup = 1 if args.warmup is None else args.warmup
