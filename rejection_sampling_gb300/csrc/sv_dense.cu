@@ -219,29 +219,89 @@ __device__ __forceinline__ uint32_t piece_element(const uint4 (&r)[4], int xl, i
   return __shfl_sync(0xffffffffu, out, owner);
 }
 
-// residual (or p) mass of a piece held in registers
-__device__ __forceinline__ float piece_resid(const uint4 (&t)[4], const uint4 (&d)[4], int bf16,
-                                             const StopInfo& st) {
-  float acc = 0.f;
+
+// ---------------------------------------------------------------------------
+// the residual pass: lane l loads vectors l + 32 i (coalesced) and sums each
+// of its four 16-byte vectors; the warp then regroups the 128 vector sums into
+// 32 run sums, run g = vectors 4 g .. 4 g + 3 (contiguous elements), the
+// prefix steps the token draw uses
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void load_run(const unsigned char* base, int ne, int bf16, int aligned,
+                                         int lane, uint4 (&r)[4]) {
+  const int epv = bf16 ? 8 : 4;
+  const uint32_t ninf = bf16 ? kNegInf2 : kNegInfF;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vi = lane + 32 * i;
+    if (aligned) {
+      r[i] = (vi * epv < ne) ? ld_stream(base + 16 * (size_t)vi) : make_uint4(ninf, ninf, ninf, ninf);
+    } else {
+      uint32_t w[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (bf16) {
+          const int e0 = vi * 8 + 2 * q;
+          const uint16_t* h = reinterpret_cast<const uint16_t*>(base);
+          const uint32_t lo = (e0 < ne) ? h[e0] : 0xFF80u;
+          const uint32_t hi = (e0 + 1 < ne) ? h[e0 + 1] : 0xFF80u;
+          w[q] = lo | (hi << 16);
+        } else {
+          const int e = vi * 4 + q;
+          w[q] = (e < ne) ? reinterpret_cast<const uint32_t*>(base)[e] : kNegInfF;
+        }
+      }
+      r[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+}
+// this lane's run of a 16-byte aligned piece -> shared memory (cp.async)
+__device__ __forceinline__ void stage_run(const unsigned char* base, int ne, int bf16, int lane,
+                                          unsigned char* dst) {
+  const int epv = bf16 ? 8 : 4;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vi = lane + 32 * i;
+    if (vi * epv < ne) cp_async16(dst + 16 * vi, base + 16 * (size_t)vi);
+  }
+}
+__device__ __forceinline__ void read_run(const unsigned char* src, int ne, int bf16, int lane,
+                                         uint4 (&r)[4]) {
+  const int epv = bf16 ? 8 : 4;
+  const uint32_t ninf = bf16 ? kNegInf2 : kNegInfF;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vi = lane + 32 * i;
+    r[i] = (vi * epv < ne) ? *reinterpret_cast<const uint4*>(src + 16 * vi) : make_uint4(ninf, ninf, ninf, ninf);
+  }
+}
+// run sum g of r (or p) on lane g: each vector summed in element order, the
+// vector sums regrouped through the warp's 512-byte scratch `vs`
+__device__ __forceinline__ float run_resid(const uint4 (&t)[4], const uint4 (&d)[4], int bf16,
+                                           const StopInfo& st, float* vs, int lane) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const uint32_t tw[4] = {t[i].x, t[i].y, t[i].z, t[i].w};
     const uint32_t dw[4] = {d[i].x, d[i].y, d[i].z, d[i].w};
+    float acc = 0.f;
     if (bf16) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         const float tv = (e & 1) ? bf16_hi(tw[e >> 1]) : bf16_lo(tw[e >> 1]);
         const float dv = (e & 1) ? bf16_hi(dw[e >> 1]) : bf16_lo(dw[e >> 1]);
-        acc += resid_val(tv, dv, st.ct, st.cd, st.invSt, st.invSd, st.mode);
+        acc = __fadd_rn(acc, resid_val(tv, dv, st.ct, st.cd, st.invSt, st.invSd, st.mode));
       }
     } else {
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        acc += resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), st.ct, st.cd, st.invSt,
-                         st.invSd, st.mode);
+        acc = __fadd_rn(acc, resid_val(__uint_as_float(tw[e]), __uint_as_float(dw[e]), st.ct,
+                                       st.cd, st.invSt, st.invSd, st.mode));
     }
+    vs[lane + 32 * i] = acc;
   }
-  return warp_sum(acc);
+  __syncwarp();
+  const float4 g = reinterpret_cast<const float4*>(vs)[lane];
+  __syncwarp();  // the scratch is reused by the next piece
+  return __fadd_rn(__fadd_rn(__fadd_rn(g.x, g.y), g.z), g.w);
 }
 
 __device__ __forceinline__ void combine_part(const UnitPart& u, float& Ct, ff& St, float& Cd,
@@ -680,7 +740,7 @@ __device__ __forceinline__ uint32_t map_rank0(const void* p) {
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
-constexpr int kMassSmem = 2048;  // pieces per row whose masses are kept on chip
+constexpr int kMassSmem = 1024;  // pieces per row whose masses are kept on chip
 
 // block-wide: the first thread with `cond` (kThreads if none) and the largest
 // `v` (one ballot / reduction per warp, then one pass over the warps; no
@@ -704,6 +764,94 @@ __device__ __forceinline__ void block_first_and_max(bool cond, int v, SelShared&
   __syncthreads();  // wa / wb may be reused
   first = f;
   vmax = m;
+}
+
+__device__ __forceinline__ float warp_inclusive_scan_f(float v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v = __fadd_rn(v, y);
+  }
+  return v;
+}
+
+constexpr int kLanePieces = 160;  // pieces per row whose lane run sums are kept on chip
+
+// The token draw from the piece masses `sm` and the lane run sums `sl` kept
+// in shared memory, by one warp: a float-float prefix over the pieces picks
+// the piece, one over its 32 run sums picks the run, an fp32 prefix over the
+// run's elements (plus the float-float base) picks the token.  Returns T; a
+// zero residual after a rejection (only through rounding) returns T = 0 and
+// draws nothing: the caller then takes the general path.
+__device__ double select_fast(const DenseParams& P, int b, const StopInfo& st, const float* sm,
+                              const float* sl, int lane) {
+  const int V = P.V, np = P.g.np, pe = P.g.pe, run = pe / 32;
+  const float us = P.u_s[b];
+  const int per = (np + 31) / 32;
+  const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
+  ff ls{0.f, 0.f};
+  for (int k = k0; k < k1; ++k) ls = ff_add_f(ls, sm[k]);
+  const ff ex = warp_exclusive_scan_ff(ls, lane);
+  const ff T = ff_shfl(ff_add(ex, ls), 31);
+  if (!(T.hi > 0.f) && st.mode == 0) return 0.0;
+  const ff target = ff_mul_f(T, us);
+  // piece level
+  const unsigned hit = __ballot_sync(0xffffffffu, (k1 > k0) && ff_gt(ff_add(ex, ls), target));
+  int kstar = 0;
+  ff base{0.f, 0.f};
+  if (hit) {
+    const int fl = __ffs(hit) - 1;
+    if (lane == fl) {
+      ff acc = ex;
+      for (int k = k0; k < k1; ++k) {
+        base = acc;
+        acc = ff_add_f(acc, sm[k]);
+        kstar = k;
+        if (ff_gt(acc, target)) break;
+      }
+    }
+    kstar = __shfl_sync(0xffffffffu, kstar, fl);
+    base = ff_shfl(base, fl);
+  } else {  // u*T at or past the total: the last piece with mass
+    int last = -1;
+    for (int k = k0; k < k1; ++k)
+      if (sm[k] > 0.f) last = k;
+    last = (int)__reduce_max_sync(0xffffffffu, (unsigned)(last + 1)) - 1;
+    kstar = last < 0 ? 0 : last;
+  }
+  // run level
+  const float lv = sl[kstar * 32 + lane];
+  const ff lbase = ff_add(base, warp_exclusive_scan_ff(ff{lv, 0.f}, lane));
+  const unsigned hit2 = hit ? __ballot_sync(0xffffffffu, ff_gt(ff_add_f(lbase, lv), target)) : 0u;
+  int fr;
+  if (hit2) {
+    fr = __ffs(hit2) - 1;
+  } else {  // the last run with mass
+    fr = (int)__reduce_max_sync(0xffffffffu, (unsigned)(lv > 0.f ? lane + 1 : 0)) - 1;
+    if (fr < 0) fr = 0;
+  }
+  // element level: lane e takes element e of run fr
+  const int y0 = kstar * pe, ne = min(pe, V - y0);
+  const int e = fr * run + lane;
+  const bool valid = lane < run && e < ne;
+  const unsigned char* trow = target_row(P, b, st.n);
+  float r = 0.f;
+  if (valid)
+    r = resid_val(logit_at(trow, y0 + e, P.bf16),
+                  st.mode == 0 ? logit_at(draft_row(P, b, st.n), y0 + e, P.bf16) : 0.f, st.ct,
+                  st.cd, st.invSt, st.invSd, st.mode);
+  const float incl = warp_inclusive_scan_f(r, lane);
+  const ff lb = ff_shfl(lbase, fr);
+  const unsigned cross = hit2 ? __ballot_sync(0xffffffffu, valid && ff_gt(ff_add_f(lb, incl), target)) : 0u;
+  int y;
+  if (cross) {
+    y = y0 + fr * run + __ffs(cross) - 1;
+  } else {  // rounding between the sums, or past the total: the run's last element with mass
+    const int lp = (int)__reduce_max_sync(0xffffffffu, (unsigned)(r > 0.f ? e + 1 : 0)) - 1;
+    y = y0 + (lp >= 0 ? lp : fr * run);
+  }
+  if (lane == 0) P.tok_out[(size_t)b * (P.G + 1) + st.n] = y;
+  return (double)T.hi + (double)T.lo;
 }
 
 // the token of row b from its piece masses `mv` (shared memory of this CTA,
@@ -824,16 +972,25 @@ __device__ double select_row(const DenseParams& P, int b, StopInfo& st, float* m
   return (double)T.hi + (double)T.lo;
 }
 
+constexpr size_t kRowWarpBuf = 2 * kPieceBytes + 512;  // a prefetched piece pair + vector sums
+constexpr size_t kRowSmem = (size_t)kWarps * kRowWarpBuf + (size_t)kLanePieces * 32 * sizeof(float);
+
 __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_constant__ DenseParams P) {
+  extern __shared__ __align__(16) unsigned char row_smem[];
   __shared__ FinShared F;
   __shared__ SelShared S;
   __shared__ float s_mass[kMassSmem];  // the row's piece masses (rank 0), when they fit
+  __shared__ double s_T;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = (int)cluster_size(), r = (int)cluster_rank();
-  const bool in_smem = P.g.np <= kMassSmem;
   const int b = blockIdx.x / C;
   const bool owner = r == 0;
   const int G = P.G, np = P.g.np, pe = P.g.pe;
+  const bool in_smem = np <= kMassSmem;   // masses on chip
+  const bool fast = np <= kLanePieces;    // lane run sums on chip too: one-warp draw
+  unsigned char* wbuf = row_smem + (size_t)warp * kRowWarpBuf;
+  float* vs = reinterpret_cast<float*>(wbuf + 2 * kPieceBytes);
+  float* s_lane = reinterpret_cast<float*>(row_smem + (size_t)kWarps * kRowWarpBuf);
   // inputs first (they do not come from the statistics kernel) ...
   for (int j = threadIdx.x; j < G; j += kThreads) {
     F.u[j] = P.u_acc[(size_t)b * G + j];
@@ -844,39 +1001,83 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
   asm volatile("griddepcontrol.wait;" ::: "memory");
   finalize_row(P, b, warp, lane, F, owner);
   StopInfo st = F.st;
-  // residual (or p) masses of this CTA's share of the stop position's pieces
+  // residual (or p) masses of this CTA's share of the stop position's pieces,
+  // two pieces per warp at a time: the second is staged by cp.async while
+  // the first is loaded straight into registers and reduced
   if (st.mode != 2) {
     const int k_lo = (int)((long long)r * np / C), k_hi = (int)((long long)(r + 1) * np / C);
     const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
-    for (int k = k_lo + warp; k < k_hi; k += kWarps) {
-      const int ne = min(pe, P.V - k * pe);
-      const size_t off = (size_t)k * kPieceBytes;
-      uint4 rt[4], rd[4];
-      load_piece(target_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rt);
-      if (st.mode == 0)
-        load_piece(draft_row(P, b, st.n) + off, ne, P.bf16, P.aligned, lane, rd);
-      else
-        for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
-      const float mass = piece_resid(rt, rd, P.bf16, st);
+    const unsigned char* trow = target_row(P, b, st.n);
+    const unsigned char* drow = (st.mode == 0) ? draft_row(P, b, st.n) : nullptr;
+    auto publish = [&](int k, float lsum) {
+      const float mass = warp_sum(lsum);
+      if (fast) st_cluster_f32(map_rank0(&s_lane[k * 32 + lane]), lsum);
       if (lane == 0) {
         if (in_smem)  // into the rank-0 CTA's shared memory
           st_cluster_f32(map_rank0(&s_mass[k]), mass);
         else
           ws_at<float>(P, P.L.rmass)[(size_t)b * P.g.np4 + k] = mass;
       }
+    };
+    for (int k = k_lo + warp; k < k_hi; k += 2 * kWarps) {
+      const int k2 = k + kWarps;
+      const bool pre = k2 < k_hi && P.aligned;
+      if (pre) {
+        const int ne2 = min(pe, P.V - k2 * pe);
+        stage_run(trow + (size_t)k2 * kPieceBytes, ne2, P.bf16, lane, wbuf);
+        if (drow) stage_run(drow + (size_t)k2 * kPieceBytes, ne2, P.bf16, lane, wbuf + kPieceBytes);
+      }
+      cp_async_commit();
+      uint4 rt[4], rd[4];
+      {
+        const int ne = min(pe, P.V - k * pe);
+        load_run(trow + (size_t)k * kPieceBytes, ne, P.bf16, P.aligned, lane, rt);
+        if (drow)
+          load_run(drow + (size_t)k * kPieceBytes, ne, P.bf16, P.aligned, lane, rd);
+        else
+          for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
+        publish(k, run_resid(rt, rd, P.bf16, st, vs, lane));
+      }
+      if (k2 < k_hi) {
+        const int ne2 = min(pe, P.V - k2 * pe);
+        if (pre) {
+          cp_async_wait_group<0>();
+          read_run(wbuf, ne2, P.bf16, lane, rt);
+          if (drow) read_run(wbuf + kPieceBytes, ne2, P.bf16, lane, rd);
+        } else {
+          load_run(trow + (size_t)k2 * kPieceBytes, ne2, P.bf16, P.aligned, lane, rt);
+          if (drow) load_run(drow + (size_t)k2 * kPieceBytes, ne2, P.bf16, P.aligned, lane, rd);
+        }
+        if (!drow)
+          for (int i = 0; i < 4; ++i) rd[i] = make_uint4(ninf, ninf, ninf, ninf);
+        publish(k2, run_resid(rt, rd, P.bf16, st, vs, lane));
+      }
     }
   }
   cluster_barrier();  // every CTA's masses are written; every record was read
   if (!owner) return;
-  double T = 0.0;
-  if (st.mode != 2)
-    T = select_row(P, b, st, in_smem ? s_mass : ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4,
-                   in_smem, S);
-  // the records, the masses and the stop record are consumed: leave the workspace zero
+  // the draw, while the other warps leave the workspace zero: the records
+  // and (off chip) the masses are consumed
   UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * np;
-  for (int i = threadIdx.x; i < (G + 1) * np; i += kThreads) zero32(up_row + i);
   float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
-  for (int k = threadIdx.x; k < np; k += kThreads) rm[k] = 0.f;
+  double T = 0.0;
+  if (fast && st.mode != 2) {
+    if (warp == 0) {
+      T = select_fast(P, b, st, s_mass, s_lane, lane);
+      if (lane == 0) s_T = T;
+    } else {
+      for (int i = threadIdx.x - 32; i < (G + 1) * np; i += kThreads - 32) zero32(up_row + i);
+    }
+    __syncthreads();
+    T = s_T;
+    if (!(T > 0.0) && st.mode == 0) T = select_row(P, b, st, s_mass, true, S);  // zero residual
+  } else {
+    if (st.mode != 2)
+      T = select_row(P, b, st, in_smem ? s_mass : rm, in_smem, S);
+    for (int i = threadIdx.x; i < (G + 1) * np; i += kThreads) zero32(up_row + i);
+  }
+  if (!in_smem)
+    for (int k = threadIdx.x; k < np; k += kThreads) rm[k] = 0.f;
   if (threadIdx.x == 0 && P.keep_stop) {  // read (and cleared) by the residual-output kernel
     st.T = T;
     ws_at<StopInfo>(P, P.L.stop)[b] = st;
@@ -921,6 +1122,9 @@ cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
     e = cudaFuncSetAttribute(dense_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStatsSmem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(dense_row_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kRowSmem);
+    if (e != cudaSuccess) return e;
     sms[dev] = n;
   }
   const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
@@ -938,7 +1142,7 @@ cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long long)p.B * C), 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = kRowSmem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
