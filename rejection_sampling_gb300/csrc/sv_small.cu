@@ -3,7 +3,8 @@
 // One warp verifies one row (dense) or one sequence window (any-order).  The
 // row block is staged in shared memory with an odd row stride, so lane i can
 // read position i's row with no bank conflicts; lane i owns position i:
-// softmax statistics of its target and draft rows, the gather at its draft
+// softmax statistics of its target and draft rows (for a few long rows the
+// warp computes them together, one row at a time), the gather at its draft
 // token and its accept test.  A ballot gives the first rejection; the whole
 // warp then draws the replacement (or the bonus token) by a float-float prefix over
 // the fp32 residual values in ascending id order.
@@ -34,21 +35,48 @@ __device__ __forceinline__ float resid_val(float t, float d, float ct, float cd,
   return r > 0.f ? r : 0.f;
 }
 
-// softmax statistics of one shared-memory row: c = log2e * max, S = sum 2^(v log2e - c)
+// softmax statistics of one shared-memory row, one lane alone:
+// c = log2e * max, S = sum 2^(v log2e - c).  Up to 256 terms the sum runs in
+// four fp32 partial sums (at most 64 terms each, so its relative error stays
+// below 64 units in the last place); longer rows are summed in float-float.
 __device__ __forceinline__ void row_stats(const float* row, int V, float& c_out, float& s_out) {
   float m = -INFINITY;
   for (int y = 0; y < V; ++y) m = fmaxf(m, row[y]);
   const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   int y = 0;
-  for (; y + 3 < V; y += 4) {
-    a0 += ex2(fmaf(row[y], kLog2e, -c));
-    a1 += ex2(fmaf(row[y + 1], kLog2e, -c));
-    a2 += ex2(fmaf(row[y + 2], kLog2e, -c));
-    a3 += ex2(fmaf(row[y + 3], kLog2e, -c));
+  if (V <= 256) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    for (; y + 3 < V; y += 4) {
+      a0 += ex2(fmaf(row[y], kLog2e, -c));
+      a1 += ex2(fmaf(row[y + 1], kLog2e, -c));
+      a2 += ex2(fmaf(row[y + 2], kLog2e, -c));
+      a3 += ex2(fmaf(row[y + 3], kLog2e, -c));
+    }
+    for (; y < V; ++y) a0 += ex2(fmaf(row[y], kLog2e, -c));
+    s_out = (a0 + a1) + (a2 + a3);
+  } else {
+    ff a0{0.f, 0.f}, a1{0.f, 0.f};
+    for (; y + 1 < V; y += 2) {
+      a0 = ff_add_f(a0, ex2(fmaf(row[y], kLog2e, -c)));
+      a1 = ff_add_f(a1, ex2(fmaf(row[y + 1], kLog2e, -c)));
+    }
+    if (y < V) a0 = ff_add_f(a0, ex2(fmaf(row[y], kLog2e, -c)));
+    s_out = ff_to_f(ff_add(a0, a1));
   }
-  for (; y < V; ++y) a0 += ex2(fmaf(row[y], kLog2e, -c));
-  s_out = (a0 + a1) + (a2 + a3);
+  c_out = (m == -INFINITY) ? -INFINITY : c;
+}
+
+// the same statistics, the whole warp on one row (lane-strided, then reduced);
+// every lane returns them
+__device__ __forceinline__ void row_stats_warp(const float* row, int V, int lane, float& c_out,
+                                               float& s_out) {
+  float m = -INFINITY;
+  for (int y = lane; y < V; y += 32) m = fmaxf(m, row[y]);
+  m = warp_max(m);
+  const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
+  ff a{0.f, 0.f};
+  for (int y = lane; y < V; y += 32) a = ff_add_f(a, ex2(fmaf(row[y], kLog2e, -c)));
+  s_out = ff_to_f(warp_sum_ff(a));
   c_out = (m == -INFINITY) ? -INFINITY : c;
 }
 
@@ -173,11 +201,27 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   const int prow = (P.flat && P.anyorder) ? sig : lane;
   float ct = 0.f, St = 1.f, cd = 0.f, Sd = 1.f, a = 0.f;
   int err = bad, acc = 1, x = 0;
+  // Lane r computes row r's statistics alone while rows are short next to
+  // their count; for few long rows the whole warp takes one row at a time
+  // (about R * (V / 32 + 20) steps instead of V).
+  const bool by_warp = R * (V + 640) < 32 * V;
+  if (!bad && by_warp) {
+    for (int r = 0; r < R; ++r) {
+      const int rr = (P.flat && P.anyorder) ? __shfl_sync(0xffffffffu, sig, r) : r;
+      float c1, s1;
+      row_stats_warp(st + rr * VS, V, lane, c1, s1);
+      if (lane == r) ct = c1, St = s1;
+      if (r < NT) {
+        row_stats_warp(sd + rr * VS, V, lane, c1, s1);
+        if (lane == r) cd = c1, Sd = s1;
+      }
+    }
+  }
   if (!bad && lane < R) {
-    row_stats(st + prow * VS, V, ct, St);
+    if (!by_warp) row_stats(st + prow * VS, V, ct, St);
     err |= !stats_ok(ct, St);
     if (lane < NT) {
-      row_stats(sd + prow * VS, V, cd, Sd);
+      if (!by_warp) row_stats(sd + prow * VS, V, cd, Sd);
       err |= !stats_ok(cd, Sd);
       x = P.anyorder ? P.x[(size_t)b * P.D + sig] : P.x[(size_t)b * NT + lane];
       if (x < 0 || x >= V) err = 1;

@@ -51,17 +51,23 @@ def dense_parity(d, min_clean=0.8, residual=True):
 
 
 # ---------------------------------------------------------------------------
-# dense, fused persistent kernel (large vocabularies)
+# dense, large vocabularies (statistics kernel + row kernel); every case here
+# has (gamma + 1) * V too large for one warp's shared-memory block, or more
+# than 32 positions
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("B,G,V,dtype", [
     (3, 7, 20000, "bf16"),     # several units per row, ragged last piece
-    (9, 1, 4096, "bf16"),      # exactly one piece per row
+    (9, 40, 1024, "bf16"),     # exactly one piece per row
     (2, 0, 50000, "bf16"),     # gamma = 0: plain categorical draw from p_0
     (1, 15, 70001, "bf16"),    # odd V: rows not 16-byte aligned -> plain-copy path
     (5, 3, 30000, "f32"),
     (4, 2, 12289, "f32"),      # odd V in fp32 (unaligned rows)
     (2, 40, 3000, "bf16"),     # gamma + 1 > 32 routes to the fused kernel
-    (70, 2, 5000, "bf16"),     # more rows than the residual lag
+    (70, 2, 5000, "bf16"),     # many rows, small clusters
+    (3, 4, 200000, "bf16"),    # 196 pieces per row: block-wide draw over on-chip masses
+    (2, 3, 530001, "f32"),     # 1036 pieces per row, unaligned: masses in the workspace
+    (1, 255, 2048, "bf16"),    # the largest gamma: 256 positions per row
+    (400, 33, 1024, "bf16"),   # more rows than SMs: one CTA per row
 ])
 def test_dense_fused_parity(B, G, V, dtype):
     d = wl.dense_inputs(B, G, V, dtype=dtype, seed=B * 1000 + G * 10 + V % 97, target_sigma=3.0,
@@ -93,6 +99,10 @@ def test_dense_b64_v128256_more_seeds(seed):
 @pytest.mark.parametrize("B,G,V,dtype", [
     (1, 4, 32, "f32"), (300, 4, 32, "f32"), (200, 31, 33, "f32"), (100, 0, 100, "bf16"),
     (64, 6, 257, "bf16"), (50, 2, 1000, "f32"),
+    (9, 1, 4096, "bf16"),      # few long rows: the warp computes each row's statistics
+    (400, 1, 4096, "bf16"),    # the same, many rows
+    (50, 30, 384, "f32"),      # one lane per row, sums over more than 256 terms
+    (3, 0, 12287, "f32"),      # the longest row one warp holds
 ])
 def test_dense_small_parity(B, G, V, dtype):
     d = wl.dense_inputs(B, G, V, dtype=dtype, seed=G * 7 + V, target_sigma=2.0, draft_noise=1.0)
