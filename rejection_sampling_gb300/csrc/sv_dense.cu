@@ -334,6 +334,7 @@ struct FinShared {
   int x[kMaxG];       // draft tokens of the row (prefetched)
   int n;              // first rejected position (G + 1: none)
   int err;
+  float us;           // u_sample of the row (prefetched)
   StopInfo st;        // the result: stop position and its draw constants
 };
 
@@ -579,6 +580,11 @@ __device__ __forceinline__ void piece_accumulate(const DenseParams& P, const Ite
 
 __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // Launched as a programmatic dependent of whatever precedes it on the
+  // stream (often the previous call's row kernel): the CTAs may be resident
+  // early, but nothing is read before that grid has completed and its
+  // memory is visible -- it may have produced these logits.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
   const long long W = (long long)P.B * (G + 1) * np;
@@ -784,9 +790,8 @@ constexpr int kLanePieces = 160;  // pieces per row whose lane run sums are kept
 // zero residual after a rejection (only through rounding) returns T = 0 and
 // draws nothing: the caller then takes the general path.
 __device__ double select_fast(const DenseParams& P, int b, const StopInfo& st, const float* sm,
-                              const float* sl, int lane) {
+                              const float* sl, float us, int lane) {
   const int V = P.V, np = P.g.np, pe = P.g.pe, run = pe / 32;
-  const float us = P.u_s[b];
   const int per = (np + 31) / 32;
   const int k0 = min(np, lane * per), k1 = min(np, k0 + per);
   ff ls{0.f, 0.f};
@@ -991,11 +996,15 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
   unsigned char* wbuf = row_smem + (size_t)warp * kRowWarpBuf;
   float* vs = reinterpret_cast<float*>(wbuf + 2 * kPieceBytes);
   float* s_lane = reinterpret_cast<float*>(row_smem + (size_t)kWarps * kRowWarpBuf);
+  // the next call's statistics kernel may be scheduled as CTAs of this one
+  // leave (it waits for this grid before it reads anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // inputs first (they do not come from the statistics kernel) ...
   for (int j = threadIdx.x; j < G; j += kThreads) {
     F.u[j] = P.u_acc[(size_t)b * G + j];
     F.x[j] = P.x[(size_t)b * G + j];
   }
+  if (threadIdx.x == 0) F.us = P.u_s[b];
   // ... then, launched as a programmatic dependent of the statistics kernel,
   // wait for it to complete (and its records to be visible)
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -1063,7 +1072,7 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
   double T = 0.0;
   if (fast && st.mode != 2) {
     if (warp == 0) {
-      T = select_fast(P, b, st, s_mass, s_lane, lane);
+      T = select_fast(P, b, st, s_mass, s_lane, F.us, lane);
       if (lane == 0) s_T = T;
     } else {
       for (int i = threadIdx.x - 32; i < (G + 1) * np; i += kThreads - 32) zero32(up_row + i);
@@ -1132,9 +1141,20 @@ cudaError_t launch_dense(const DenseParams& p, cudaStream_t s) {
   if (grid * kStatsWarps > pieces) grid = (pieces + kStatsWarps - 1) / kStatsWarps;
   DenseParams q = p;
   q.stats_warps = grid * kStatsWarps;
-  dense_stats_kernel<<<(unsigned)grid, kStatsThreads, kStatsSmem, s>>>(q);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  {
+    cudaLaunchConfig_t k1 = {};
+    k1.gridDim = dim3((unsigned)grid, 1, 1);
+    k1.blockDim = dim3(kStatsThreads, 1, 1);
+    k1.dynamicSmemBytes = kStatsSmem;
+    k1.stream = s;
+    cudaLaunchAttribute a1[1];
+    a1[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a1[0].val.programmaticStreamSerializationAllowed = 1;
+    k1.attrs = a1;
+    k1.numAttrs = 1;
+    e = cudaLaunchKernelEx(&k1, dense_stats_kernel, q);
+    if (e != cudaSuccess) return e;
+  }
   // clusters of C CTAs per row: about two CTAs per SM in all, at most 8
   int C = (int)((2ll * sms[dev]) / p.B);
   C = C < 1 ? 1 : (C > 8 ? 8 : C);
