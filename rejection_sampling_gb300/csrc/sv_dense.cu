@@ -1064,27 +1064,32 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
     }
   }
   cluster_barrier();  // every CTA's masses are written; every record was read
-  if (!owner) return;
-  // the draw, while the other warps leave the workspace zero: the records
-  // and (off chip) the masses are consumed
   UnitPart* up_row = ws_at<UnitPart>(P, P.L.upart) + (size_t)b * (G + 1) * np;
+  const int nrec = (G + 1) * np;
+  if (!owner) {
+    // ranks 1 .. C-1 leave the row's records zero while rank 0 draws (its
+    // warps' loads would otherwise queue behind these stores)
+    const int lo = (int)((long long)(r - 1) * nrec / (C - 1));
+    const int hi = (int)((long long)r * nrec / (C - 1));
+    for (int i = lo + (int)threadIdx.x; i < hi; i += kThreads) zero32(up_row + i);
+    return;
+  }
+  // the draw; the masses kept off chip are consumed
   float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
   double T = 0.0;
   if (fast && st.mode != 2) {
     if (warp == 0) {
       T = select_fast(P, b, st, s_mass, s_lane, F.us, lane);
       if (lane == 0) s_T = T;
-    } else {
-      for (int i = threadIdx.x - 32; i < (G + 1) * np; i += kThreads - 32) zero32(up_row + i);
     }
     __syncthreads();
     T = s_T;
     if (!(T > 0.0) && st.mode == 0) T = select_row(P, b, st, s_mass, true, S);  // zero residual
-  } else {
-    if (st.mode != 2)
-      T = select_row(P, b, st, in_smem ? s_mass : rm, in_smem, S);
-    for (int i = threadIdx.x; i < (G + 1) * np; i += kThreads) zero32(up_row + i);
+  } else if (st.mode != 2) {
+    T = select_row(P, b, st, in_smem ? s_mass : rm, in_smem, S);
   }
+  if (C == 1)
+    for (int i = threadIdx.x; i < nrec; i += kThreads) zero32(up_row + i);
   if (!in_smem)
     for (int k = threadIdx.x; k < np; k += kThreads) rm[k] = 0.f;
   if (threadIdx.x == 0 && P.keep_stop) {  // read (and cleared) by the residual-output kernel
