@@ -422,7 +422,7 @@ def run_ours(args):
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "frac_of_nominal_8TBps": achieved / NOMINAL_HBM_GBS,
                          "traffic": traffic, "algorithmic_bytes_per_launch": nbytes,
-                         "kernel": "dense_stats_kernel + dense_resid_kernel (one call)", "mean_launch_us": kernel_ms * 1e3},
+                         "kernel": "dense_stats_kernel + dense_row_kernel (one call)", "mean_launch_us": kernel_ms * 1e3},
             "cpu_baseline": cpu,
             "e2e": e2e,
             "gpu_launches": 2 * args.steps,  # dense_stats_kernel + dense_row_kernel per call

@@ -28,12 +28,15 @@
  * Conventions for every entry point
  *   - All pointers are DEVICE pointers owned by the caller (cudaMalloc,
  *     cudaMallocAsync or a framework allocator); the library allocates no
- *     memory and keeps no global state.  Calls are asynchronous on `stream`
- *     (the legacy default stream if 0).
+ *     memory.  Its only state is a per-device cache of launch attributes (set
+ *     on the first call on each device) and, for spec_verify_dense_static
+ *     alone, a fixed device scratch array.  Calls are asynchronous on
+ *     `stream` (the legacy default stream if 0).
  *   - Tensors are dense, row-major, contiguous, with the shapes given below.
  *     int32 / fp32 arrays need 4-byte alignment, bf16 arrays 2-byte
  *     alignment.  Logit rows whose byte length is a multiple of 16, with
- *     16-byte aligned base pointers, take the bulk-copy (TMA) fast path.
+ *     16-byte aligned base pointers, take the fast path (16-byte cp.async
+ *     copies into shared memory); other rows are read element by element.
  *   - Host-side argument errors (null pointers, non-positive sizes, sizes out
  *     of range, a workspace that is too small) return SV_ERR_INVALID_ARG
  *     synchronously and launch nothing.  A failed launch returns SV_ERR_CUDA.
@@ -42,9 +45,13 @@
  *     contains NaN or +inf or is entirely -inf) do not stop the call: the
  *     offending row gets n_accepted = -1 and out_tokens = -1, and a bit is
  *     set in the workspace status word that spec_verify_check() reports.
- *   - No kernel waits on another thread block: work is handed on by
- *     per-row arrival counters.  (SV_ERR_TIMEOUT is kept for ABI stability;
- *     this version never reports it.)
+ *   - Waits between thread blocks are only the hardware's: the dense call's
+ *     second kernel is a programmatic dependent of the first
+ *     (griddepcontrol.wait) and its CTAs meet at cluster barriers; the first
+ *     kernel is a programmatic dependent of whatever precedes it on the
+ *     stream and reads nothing before that grid has completed.  No kernel
+ *     spins on memory written by another block.  (SV_ERR_TIMEOUT is kept for
+ *     ABI stability; this version never reports it.)
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H

@@ -1,6 +1,4 @@
-// sv_dense.cu -- dense verification for large vocabularies: two streaming
-// kernels, one HBM pass over every logit plus one pass over the two rows of
-// each row's stop position.
+// sv_dense.cu -- dense verification for large vocabularies.
 //
 // Computes, for every row b (DFlash/DFlash2 guide, 4.4; Uno article, "What
 // 'lossless' actually has to mean"):
@@ -10,36 +8,40 @@
 //   token n = inverse CDF of max(p_n - q_n, 0) (n < gamma) or of p_gamma
 //   (bonus, DFlash/DFlash2 guide section 2) at u_sample[b].
 //
-// Design.
-//  * A logit row is cut into 2 KB pieces; a CTA of 16 warps takes 16
-//    consecutive pieces (a 32 KB chunk), one warp per piece.
-//  * dense_stats_kernel: one CTA per (row b, position j, chunk c), launched
-//    row by row.  Each warp loads its target piece and the same draft piece
-//    straight into registers (16-byte loads, all in flight together), reduces
-//    each to (c, S) -- c = log2e * max (max.bf16x2), S = sum 2^(v log2e - c)
-//    (ex2.approx) -- and the warp holding the draft token x_j picks up the two
-//    logits there.  Warp 0 combines the 16 pieces in float-float and writes
-//    the chunk's partial.  The CTA that completes a row (a per-row arrival
-//    counter) finalises it: combines every position's partials, forms the
-//    ratios, runs the accept tests, finds n and writes the stop record, the
-//    accept probabilities and every token but the one drawn at n.  Rows
-//    complete in launch order, so all but the last rows' finalisations
-//    overlap the stream of later rows.
-//  * dense_resid_kernel: one CTA per (row b, chunk c) recomputes
-//    r(y) = max(p_n(y) - q_n(y), 0) (or p_gamma) over its chunk of the stop
-//    position's two rows and writes one mass per piece.  The CTA completing
-//    the row draws the token: a float-float prefix over the piece masses picks
-//    the piece, then a prefix over the piece's fp32 values picks y.
-//  * No thread ever waits for another CTA: hand-offs are last-arriver
-//    counters, which the finishing CTA resets, and every array a call reads is
-//    written earlier in the same call.  The workspace is all zero again after
-//    every call.
+// Design (two kernels per call, one HBM pass over every logit plus a second
+// read of each row's stop position).
+//  * A logit row is cut into 2 KB pieces; piece (b, j, k) pairs target piece
+//    k of row-position (b, j) with the same draft piece.
+//  * dense_stats_kernel: a persistent grid, one CTA of 24 warps per SM.
+//    Every warp takes one contiguous range of pieces (in (b, j, k) order) and
+//    streams it through a private two-stage ring of 4 KB shared-memory stages
+//    filled by 16-byte cp.async.  Per piece it forms c = log2e * max
+//    (max.bf16x2) and S = sum 2^(v log2e - c) (ex2.approx) for the target and
+//    the draft piece and folds them into the running statistics of the
+//    (b, j) segment it is in; the piece holding the draft token also gives
+//    the two logits there.  Each segment of a range ends in one 32-byte record
+//    at the segment's first piece.
+//  * dense_row_kernel: one thread-block cluster of C CTAs per row, launched
+//    as a programmatic dependent of the statistics kernel.  Every CTA finds
+//    the row's records from the statistics warps' ranges, combines them per
+//    position (float-float), forms p/q at the draft token, runs the accept
+//    tests and takes the first rejection n and the draw constants.  Each CTA
+//    then computes the residual (or p) mass of its share of the stop
+//    position's pieces, with 32 run sums per piece, into the rank-0 CTA's
+//    shared memory (st.shared::cluster).  After a cluster barrier one warp of
+//    rank 0 draws the token -- float-float prefixes over the piece masses and
+//    the chosen piece's run sums, then an fp32 prefix over the chosen run's
+//    elements -- while the other CTAs clear the row's records.
+//  * The statistics kernel is itself a programmatic dependent of whatever
+//    precedes it and waits before it reads anything, so back-to-back calls do
+//    not pay its launch latency.  The workspace is all zero again after every
+//    call.
 #include "sv_common.cuh"
 
 namespace sv {
 namespace {
 
-constexpr int kWarps = kChunkPieces;  // warps per CTA, one piece each
+constexpr int kWarps = 16;  // warps per row-kernel CTA
 constexpr int kThreads = 32 * kWarps;
 constexpr int kMaxG = 256;            // positions per row (gamma + 1 <= 256)
 

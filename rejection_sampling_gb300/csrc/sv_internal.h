@@ -25,14 +25,12 @@ static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 // dense kernels: geometry and workspace layout
 // ---------------------------------------------------------------------------
 constexpr int kPieceBytes = 2048;  // one warp's slice of a logit row
-constexpr int kChunkPieces = 16;   // pieces per CTA (one per warp): a 32 KB chunk per row
 
 struct DenseGeom {
   int es;   // element size in bytes (2: bf16, 4: fp32)
   int pe;   // elements per piece
   int np;   // pieces per row
   int np4;  // np rounded up to a multiple of 4 (16-byte aligned rows of masses)
-  int nc;   // chunks (CTAs) per row
 };
 
 inline DenseGeom dense_geom(int V, int es) {
@@ -41,7 +39,6 @@ inline DenseGeom dense_geom(int V, int es) {
   g.pe = kPieceBytes / es;
   g.np = (V + g.pe - 1) / g.pe;
   g.np4 = (g.np + 3) / 4 * 4;
-  g.nc = (g.np + kChunkPieces - 1) / kChunkPieces;
   return g;
 }
 
