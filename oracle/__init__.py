@@ -60,7 +60,9 @@ def _load():
             lib.oracle_verify_dense.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P, P, I]
             lib.oracle_verify_sparse.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, P, P, P, P, P, P, I]
             lib.oracle_verify_anyorder.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, P, P, P, P, P, I]
-            for f in (lib.oracle_verify_dense, lib.oracle_verify_sparse, lib.oracle_verify_anyorder):
+            lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, I]
+            for f in (lib.oracle_verify_dense, lib.oracle_verify_sparse, lib.oracle_verify_anyorder,
+                      lib.oracle_verify_greedy):
                 f.restype = I
             lib.oracle_default_threads.restype = I
             _lib = lib
@@ -114,6 +116,22 @@ def verify_dense(target, draft, draft_ids, u_accept, u_sample, *, residual=True,
         _ptr(out["accept_prob"]), _ptr(out["resid_mass"]), _ptr(out["flags"]), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_verify_dense failed")
+    return out
+
+
+def verify_greedy(target, draft_ids, *, nthreads: int = 0) -> dict:
+    """Greedy (T = 0) verification of B rows.  target [B, g+1, V]; draft_ids [B, g].
+    DFlash/DFlash2 guide, 4.4 (greedy decoding); the C file states the reading."""
+    lib = _load()
+    lt, dt = _logits(target)
+    B, G1, V = lt.shape
+    G = G1 - 1
+    x = np.ascontiguousarray(draft_ids, dtype=np.int32).reshape(B, G)
+    out = dict(n_accepted=np.zeros(B, np.int32), out_tokens=np.zeros((B, G + 1), np.int32))
+    rc = lib.oracle_verify_greedy(_ptr(lt), dt, _ptr(x), B, G, V, _ptr(out["n_accepted"]),
+                                  _ptr(out["out_tokens"]), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_verify_greedy failed")
     return out
 
 

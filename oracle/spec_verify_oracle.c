@@ -18,6 +18,9 @@
  *         is drawn from the normalised residual.
  *  [DF2]  same guide, section 2 "Speculative Decoding Speedup Formulation":
  *         tau in [1, gamma + 1] including the target's bonus token.
+ *  [DF4g] same guide, 4.4: under greedy decoding (T = 0) a draft token is
+ *         accepted if and only if a condition holds whose formula did not
+ *         survive on the page (see oracle_verify_greedy for the reading).
  *  [SSMD] "Self-Speculative Masked Diffusions", key design 2: verification
  *         in sigma order from the first unknown position; at the first
  *         rejection resample from max(0, target - draft) and end the round.
@@ -537,4 +540,81 @@ int oracle_verify_anyorder(const void* target_logits, const void* draft_logits, 
                      V,             n_accepted,   out_tokens, residual_out, accept_prob,
                      resid_mass,    flags};
   return run_rows(anyorder_row, &a, B, 3 * (size_t)V, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Greedy (T = 0)                                                        */
+/* ------------------------------------------------------------------ */
+/* [DF4g] Reading: the limit T -> 0 of the stochastic rule.  As T -> 0,
+ * p_k = softmax(target[k] / T) becomes the point mass at a_k = argmax_y
+ * target[k, y] (the smallest such y when several ids share the maximum), so
+ *  - x_k is accepted iff x_k = a_k (then p_k(x_k) = 1 >= q_k(x_k); otherwise
+ *    p_k(x_k) = 0 and the ratio is 0);
+ *  - the block stops at the first k with x_k != a_k, and the replacement,
+ *    drawn from max(p_k - q_k, 0) normalised, is the point mass at a_k;
+ *  - if every draft is accepted the bonus is a_gamma.
+ * No uniform is consumed.  Input errors as in the dense rule (NaN, +inf or
+ * an all -inf target row, a draft id out of range). */
+typedef struct {
+  const void* lt;
+  int dtype;
+  const int32_t* x;
+  int B, G, V;
+  int32_t *n_out, *tok_out;
+} greedy_args;
+
+static int argmax_row(const void* base, int dtype, size_t off, int V) {
+  int best = 0;
+  double bv = widen(base, dtype, off);
+  for (int y = 1; y < V; ++y) {
+    double v = widen(base, dtype, off + (size_t)y);
+    if (v > bv) {
+      bv = v;
+      best = y;
+    }
+  }
+  return best;
+}
+
+static void greedy_row(const void* pa, int b, double* scratch) {
+  const greedy_args* a = (const greedy_args*)pa;
+  const int G = a->G, V = a->V;
+  (void)scratch;
+  const size_t trow = (size_t)b * (size_t)(G + 1);
+  const size_t drow = (size_t)b * (size_t)G;
+  int32_t* tok = a->tok_out + (size_t)b * (size_t)(G + 1);
+  int bad = 0;
+  for (int j = 0; j <= G && !bad; ++j)
+    bad |= check_row(a->lt, a->dtype, (trow + j) * (size_t)V, V);
+  for (int j = 0; j < G && !bad; ++j) {
+    int32_t xj = a->x[drow + j];
+    if (xj < 0 || xj >= V) bad = -1;
+  }
+  if (bad) {
+    a->n_out[b] = -1;
+    for (int j = 0; j <= G; ++j) tok[j] = -1;
+    return;
+  }
+  int n = G;
+  for (int j = 0; j < G; ++j)
+    if (a->x[drow + j] != argmax_row(a->lt, a->dtype, (trow + j) * (size_t)V, V)) {
+      n = j;
+      break;
+    }
+  a->n_out[b] = n;
+  for (int j = 0; j < n; ++j) tok[j] = a->x[drow + j];
+  tok[n] = argmax_row(a->lt, a->dtype, (trow + n) * (size_t)V, V);
+  for (int j = n + 1; j <= G; ++j) tok[j] = -1;
+}
+
+int oracle_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_ids, int B,
+                         int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                         int nthreads) {
+  if (B < 0 || gamma < 0 || V <= 0) return -1;
+  if (B == 0) return 0;
+  if (!target_logits || !n_accepted || !out_tokens) return -1;
+  if (gamma > 0 && !draft_ids) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  greedy_args a = {target_logits, dtype, draft_ids, B, gamma, V, n_accepted, out_tokens};
+  return run_rows(greedy_row, &a, B, 1, nthreads);
 }

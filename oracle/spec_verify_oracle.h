@@ -101,6 +101,18 @@ int oracle_verify_anyorder(const void* target_logits, const void* draft_logits, 
                            double* accept_prob, double* resid_mass, uint32_t* flags,
                            int nthreads);
 
+/* Greedy (T = 0) verification ("DFlash/DFlash2 guide", 4.4: under greedy
+ * decoding a draft token is accepted if and only if it is the target's
+ * choice; the condition's formula is lost from the page, and the reading
+ * taken is the T -> 0 limit of the stochastic rule, see the .c file).
+ *   target_logits [B, gamma+1, V] (dtype), draft_ids [B, gamma];
+ *   n_accepted [B] (-1 on an input error), out_tokens [B, gamma+1]
+ *   (x_0..x_{n-1}, the target argmax at n, then -1).
+ */
+int oracle_verify_greedy(const void* target_logits, int dtype, const int32_t* draft_ids, int B,
+                         int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                         int nthreads);
+
 /* Threads the oracle would use for nthreads <= 0 (all online host cores). */
 int oracle_default_threads(void);
 

@@ -36,8 +36,8 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "bf16_bits", "bf16_bits_to_f32", "gumbel_argmax", "dense_inputs", "sparse_inputs",
-    "anyorder_inputs", "WORKLOADS", "make",
+    "bf16_bits", "bf16_bits_to_f32", "gumbel_argmax", "dense_inputs", "greedy_inputs",
+    "sparse_inputs", "anyorder_inputs", "WORKLOADS", "make",
 ]
 
 
@@ -144,6 +144,29 @@ def dense_inputs(B: int, gamma: int, V: int, *, dtype: str = "bf16", seed: int =
                 target=np.ascontiguousarray(lt_q), draft=np.ascontiguousarray(ld_q),
                 draft_ids=np.ascontiguousarray(draft_ids, dtype=np.int32),
                 u_accept=_uniform_f32(rng, (Bt, gamma)), u_sample=_uniform_f32(rng, (Bt,)))
+
+
+def greedy_inputs(B: int, gamma: int, V: int, *, dtype: str = "bf16", seed: int = 0,
+                  target_sigma: float = 3.0, draft_noise: float = 0.5) -> dict:
+    """Greedy (T = 0) verification inputs.
+
+    target [B, gamma+1, V] ~ N(0, target_sigma^2); a greedy drafter's ids:
+    draft_ids[b, j] = the id of the largest draft logit, the draft logits being
+    the target's + N(0, draft_noise^2) (a drafter that agrees with the target
+    up to noise).  No uniforms: greedy verification consumes none.
+    """
+    rng = np.random.default_rng(seed)
+    lt = rng.normal(0.0, target_sigma, size=(B, gamma + 1, V)).astype(np.float32)
+    ld = (lt[:, :gamma] + rng.normal(0.0, draft_noise, size=(B, gamma, V))).astype(np.float32)
+    if dtype == "bf16":
+        lt_q, ld_q = bf16_bits(lt), bf16_bits(ld)
+    elif dtype == "f32":
+        lt_q, ld_q = lt, ld
+    else:
+        raise ValueError(dtype)
+    draft_ids = np.argmax(_as_f64(ld_q), axis=-1).astype(np.int32) if gamma else np.zeros((B, 0), np.int32)
+    return dict(kind="greedy", dtype=dtype, B=B, gamma=gamma, V=V,
+                target=np.ascontiguousarray(lt_q), draft_ids=np.ascontiguousarray(draft_ids))
 
 
 # ---------------------------------------------------------------------------
