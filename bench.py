@@ -214,7 +214,8 @@ def variant_lines(dev, stream):
     import rejection_sampling_gb300 as rs
     from rejection_sampling_gb300 import workloads as wl
     out = {}
-    for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33"):
+    for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33",
+                 "greedy_b64_g7_v128256"):
         d = wl.make(name, seed=0)
         copies = 8  # rotate over copies so the inputs exceed L2 where they are small
         calls = []
@@ -229,6 +230,17 @@ def variant_lines(dev, stream):
                 o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
                 calls.append(rs.prepare_dense(*args, out=o, stream=stream))
+        elif d["kind"] == "greedy":
+            B, G, V = d["B"], d["gamma"], d["V"]
+            nbytes = B * (G + 1) * V * (2 if d["dtype"] == "bf16" else 4)  # target logits only
+            positions = B * G
+            copies = 2  # 2 x 131 MB > L2
+            base = [to_dev(d[k], dev) for k in ("target", "draft_ids")]
+            for c in range(copies):
+                args = [t.clone() for t in base]
+                o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
+                                    torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
+                calls.append(rs.prepare_greedy(*args, out=o, stream=stream))
         elif d["kind"] == "sparse":
             B, G, k = d["B"], d["gamma"], d["kt"]
             nbytes = B * ((G + 1) * k + G * k) * 8 + B * G * 8 + B * 4
@@ -256,6 +268,9 @@ def variant_lines(dev, stream):
                      "positions_per_s": positions / (ms * 1e-3),
                      "GBps": nbytes / (ms * 1e-3) / 1e9,
                      "bytes_per_call": nbytes}
+        if d["kind"] == "greedy":  # a streaming pass over the target logits: HBM roofline
+            peak, _ = measured_peak()
+            out[name]["frac_of_measured_hbm"] = out[name]["GBps"] / peak
         del calls
     torch.cuda.synchronize()
     return out

@@ -180,6 +180,26 @@ int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv
                          sv_stream_t stream);
 
 /*
+ * spec_verify_greedy -- greedy (temperature 0) verification (DFlash/DFlash2
+ * guide, 4.4: under greedy decoding a draft token is accepted if and only if
+ * it is the target's choice; the page's formula is lost, and this is the
+ * T -> 0 limit of spec_verify_dense's rule).  With a_j = the id of the
+ * largest target logit at position j (the smallest such id on ties):
+ *   n = the first j < gamma with draft_ids[b, j] != a_j, gamma if none;
+ *   out_tokens[b] = x_0 .. x_{n-1}, a_n, then -1 (a_gamma is the bonus token
+ *   when every draft is accepted; DFlash/DFlash2 guide, section 2).
+ *   target_logits [B, gamma+1, V] (fp32 or bf16); draft_ids [B, gamma] int32.
+ * No uniforms and no draft logits are read.  Outputs: n_accepted [B] in
+ * [0, gamma] (-1: a target row with NaN, +inf or no finite logit, or a draft
+ * id out of range; every token of the row is then -1).  Workspace: as for
+ * spec_verify_dense, spec_verify_workspace_size(B, gamma, V) bytes, zero
+ * again after the call.  Limits as spec_verify_dense.
+ */
+int spec_verify_greedy(const void* target_logits, sv_dtype dtype, const int32_t* draft_ids,
+                       int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                       void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/*
  * spec_verify_check -- synchronise `stream`, read and clear the workspace
  * status word.  Returns SV_OK, SV_ERR_DEVICE_INPUT (some row of an earlier
  * call had invalid inputs; those rows carry n_accepted = -1),

@@ -26,7 +26,7 @@ SV_F32, SV_BF16 = 0, 1
 EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
-    "spec_verify_status_string", "spec_verify_dense_static",
+    "spec_verify_status_string", "spec_verify_dense_static", "spec_verify_greedy",
 )
 
 
@@ -74,6 +74,8 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_check.argtypes = [P, Z, P]
         lib.spec_verify_status_string.restype = ctypes.c_char_p
         lib.spec_verify_status_string.argtypes = [I]
+        lib.spec_verify_greedy.restype = I
+        lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
         lib.spec_verify_dense_static.restype = I
         lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         _lib = lib
@@ -198,6 +200,51 @@ def spec_verify_dense(target_logits: torch.Tensor, draft_logits: torch.Tensor,
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_dense")
     return out
+
+
+def spec_verify_greedy(target_logits: torch.Tensor, draft_ids: torch.Tensor, *,
+                       out: Optional[VerifyResult] = None,
+                       stream: Optional[torch.cuda.Stream] = None) -> VerifyResult:
+    """Greedy (T = 0) verification.  target [B, g+1, V] (bf16 or fp32, CUDA),
+    draft_ids [B, g] int32.  Returns n_accepted and out_tokens."""
+    lib = load()
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_greedy needs CUDA tensors")
+    dt = _logit_dtype(target_logits)
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    _req(target_logits, "target_logits", target_logits.dtype, (B, G + 1, V), dev)
+    _req(draft_ids, "draft_ids", torch.int32, (B, G), dev)
+    if out is None:
+        out = VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
+                           torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, G, V), dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_greedy(_ptr(target_logits), dt, _ptr(draft_ids) if G > 0 else None,
+                                    B, G, V, _ptr(out.n_accepted), _ptr(out.out_tokens),
+                                    ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_greedy")
+    return out
+
+
+def prepare_greedy(target_logits, draft_ids, out: VerifyResult,
+                   stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """Validate once (by running the checked call) and return a PreparedCall
+    that repeats spec_verify_greedy on the same buffers."""
+    spec_verify_greedy(target_logits, draft_ids, out=out, stream=stream)
+    lib = load()
+    dev = target_logits.device
+    B, G1, V = target_logits.shape
+    G = G1 - 1
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, G, V), dev, sp)
+    args = (_ptr(target_logits), _logit_dtype(target_logits), _ptr(draft_ids) if G > 0 else None,
+            B, G, V, _ptr(out.n_accepted), _ptr(out.out_tokens), ws.data_ptr(), ws.numel(), sp)
+    keep = (target_logits, draft_ids, out, ws)
+    return PreparedCall(lib.spec_verify_greedy, args, keep, "spec_verify_greedy")
 
 
 def spec_verify_dense_static(target_logits: torch.Tensor, draft_logits: torch.Tensor,

@@ -124,6 +124,39 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
   return SV_OK;
 }
 
+int spec_verify_greedy(const void* target_logits, sv_dtype dtype, const int32_t* draft_ids,
+                       int B, int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
+                       void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !n_accepted || !out_tokens || !workspace) return SV_ERR_INVALID_ARG;
+  if (gamma > 0 && !draft_ids) return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(target_logits, es) || !aligned_to(n_accepted, 4) || !aligned_to(out_tokens, 4) ||
+      (draft_ids && !aligned_to(draft_ids, 4)) || !aligned_to(workspace, 256))
+    return SV_ERR_INVALID_ARG;
+  const sv::DenseGeom g = sv::dense_geom(V, es);
+  const sv::DenseLayout L = sv::dense_layout(B, gamma, g);
+  if (ws_bytes < L.total) return SV_ERR_INVALID_ARG;
+  if ((long long)B * (gamma + 1) * g.np >= (1ll << 31) - 1) return SV_ERR_INVALID_ARG;
+  sv::DenseParams p;
+  memset(&p, 0, sizeof p);
+  p.lt = static_cast<const unsigned char*>(target_logits);
+  p.x = draft_ids;
+  p.n_out = n_accepted;
+  p.tok_out = out_tokens;
+  p.ws = static_cast<unsigned char*>(workspace);
+  p.L = L;
+  p.g = g;
+  p.B = B;
+  p.G = gamma;
+  p.V = V;
+  p.bf16 = (dtype == SV_BF16);
+  p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(target_logits, 16);
+  return launch_status(sv::launch_greedy(p, (cudaStream_t)stream));
+}
+
 int spec_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,
                        const int32_t* drf_ids, const float* drf_probs, int kd,
                        const int32_t* draft_tokens, const float* u_accept, const float* u_sample,

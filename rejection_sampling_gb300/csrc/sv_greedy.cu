@@ -1,0 +1,401 @@
+// sv_greedy.cu -- greedy (T = 0) verification for any vocabulary size.
+//
+// Under greedy decoding a draft token is accepted if and only if it is the
+// target's own choice (DFlash/DFlash2 guide, 4.4; the condition's formula did
+// not survive on the page, and the reading taken is the T -> 0 limit of the
+// stochastic rule of the Uno article, "What 'lossless' actually has to
+// mean"): with a_j = argmax_y target[b, j, y] (the smallest such y when ids
+// tie),
+//   n       = first j < gamma with x_j != a_j (gamma if none),
+//   token n = a_n (the replacement, or the bonus a_gamma when n = gamma;
+//             DFlash/DFlash2 guide, section 2).
+// Only the target logits are read; no uniform is consumed.
+//
+// Design (two kernels per call, one HBM pass over the target logits).
+//  * A target row is cut into 2 KB pieces, numbered (b, j, k) row-major.
+//  * greedy_stats_kernel: a persistent grid, one CTA of 24 warps per SM;
+//    every warp takes one contiguous range of pieces and streams it through
+//    a private three-stage ring of 2 KB shared-memory stages filled by
+//    16-byte cp.async (plain loads when rows are not 16-byte aligned).  Each
+//    piece is reduced to (max, first index of the max, bad) -- bad: the piece
+//    holds a NaN or +inf -- and folded into the running values of the
+//    (b, j) segment the warp is in; each segment of a range ends in one
+//    record at its first piece.
+//  * greedy_row_kernel: one CTA per row, a programmatic dependent of the
+//    statistics kernel.  A warp per position combines the position's records
+//    (found from the statistics warps' ranges), giving a_j; the first
+//    mismatch and the tokens follow.  The CTA clears the records it read, so
+//    the workspace is all zero again after the call.
+#include <climits>
+
+#include "sv_common.cuh"
+
+namespace sv {
+namespace {
+
+constexpr int kGWarps = 24;  // warps per statistics CTA
+constexpr int kGThreads = 32 * kGWarps;
+constexpr int kGStages = 3;  // ring depth per warp (2 KB stages)
+constexpr size_t kGSmem = (size_t)kGWarps * kGStages * kPieceBytes;
+constexpr int kGRowWarps = 16;  // warps per row CTA
+constexpr int kGMaxPos = 256;   // positions per row (gamma + 1 <= 256)
+constexpr uint32_t kNegInf2 = 0xFF80FF80u;  // two bf16 -inf
+constexpr uint32_t kNegInfF = 0xFF800000u;  // fp32 -inf
+
+// one segment's running argmax (16 bytes, at the segment's first piece slot)
+struct ArgRec {
+  float m;   // maximum
+  int idx;   // first id holding it (INT_MAX while the maximum is -inf)
+  int bad;   // a NaN or +inf was seen
+  int pad;
+};
+
+__device__ __forceinline__ const unsigned char* target_row(const DenseParams& P, int b, int j) {
+  return P.lt + ((size_t)b * (P.G + 1) + j) * (size_t)P.V * P.g.es;
+}
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem_dst)),
+               "l"(gmem_src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// this lane's 16-byte vectors lane + 32 i of a 2 KB piece with `ne` valid
+// elements; elements past `ne` read as -inf
+__device__ __forceinline__ void load_vectors(const unsigned char* base, int ne, int bf16,
+                                             int aligned, int lane, uint4 (&r)[4]) {
+  const int epv = bf16 ? 8 : 4;
+  const uint32_t ninf = bf16 ? kNegInf2 : kNegInfF;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vi = lane + 32 * i;
+    if (aligned) {
+      r[i] = (vi * epv < ne) ? __ldcs(reinterpret_cast<const uint4*>(base) + vi)
+                             : make_uint4(ninf, ninf, ninf, ninf);
+      continue;
+    }
+    uint32_t w[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (bf16) {
+        const int e0 = vi * 8 + 2 * q;
+        const uint16_t* h = reinterpret_cast<const uint16_t*>(base);
+        const uint32_t lo = (e0 < ne) ? h[e0] : 0xFF80u;
+        const uint32_t hi = (e0 + 1 < ne) ? h[e0 + 1] : 0xFF80u;
+        w[q] = lo | (hi << 16);
+      } else {
+        const int e = vi * 4 + q;
+        w[q] = (e < ne) ? reinterpret_cast<const uint32_t*>(base)[e] : kNegInfF;
+      }
+    }
+    r[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+// (max, first index of the max, bad) of a piece, on every lane.  Element
+// e of vector vi is id vi * epv + e of the piece; a lane visits its ids in
+// increasing order and keeps the first maximum, the warp keeps the smallest
+// id among equal maxima.  NaN never compares greater, so it is never chosen;
+// it (and +inf) marks the piece bad.
+__device__ __forceinline__ void piece_argmax(const uint4 (&r)[4], int bf16, int lane, float& m,
+                                             int& idx, int& bad) {
+  const int epv = bf16 ? 8 : 4;
+  float bv = -INFINITY;
+  int bi = INT_MAX, bd = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+    const int id0 = (lane + 32 * i) * epv;
+    if (bf16) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float v = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+        bd |= (v != v) || (v == INFINITY);
+        if (v > bv) {
+          bv = v;
+          bi = id0 + e;
+        }
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float v = __uint_as_float(w[e]);
+        bd |= (v != v) || (v == INFINITY);
+        if (v > bv) {
+          bv = v;
+          bi = id0 + e;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (ov > bv || (ov == bv && oi < bi)) {
+      bv = ov;
+      bi = oi;
+    }
+  }
+  m = bv;
+  idx = bi;
+  bad = __any_sync(0xffffffffu, bd);
+}
+
+struct GItem {  // piece k of row-position (b, j)
+  int b, j, k;
+};
+__device__ __forceinline__ GItem gitem_at(long long w, int G, int np) {
+  const long long r = w / np;
+  GItem it;
+  it.k = (int)(w - r * np);
+  it.b = (int)(r / (G + 1));
+  it.j = (int)(r - (long long)it.b * (G + 1));
+  return it;
+}
+__device__ __forceinline__ void gitem_next(GItem& it, int G, int np) {
+  if (++it.k == np) {
+    it.k = 0;
+    if (++it.j == G + 1) {
+      it.j = 0;
+      ++it.b;
+    }
+  }
+}
+
+struct GSeg {
+  long long w0;  // record slot: the segment's first piece
+  int b, j;
+  float m;
+  int idx, bad;
+};
+__device__ __forceinline__ void gseg_begin(GSeg& s, const GItem& it, long long w) {
+  s.w0 = w;
+  s.b = it.b;
+  s.j = it.j;
+  s.m = -INFINITY;
+  s.idx = INT_MAX;
+  s.bad = 0;
+}
+__device__ __forceinline__ void gseg_write(const DenseParams& P, const GSeg& s, int lane) {
+  if (lane == 0) {
+    ArgRec* rec = reinterpret_cast<ArgRec*>(P.ws + P.L.upart) + s.w0;
+    *reinterpret_cast<int4*>(rec) = make_int4(__float_as_int(s.m), s.idx, s.bad, 0);
+  }
+}
+// fold piece `it` into the segment; pieces arrive in increasing id order, so
+// a strictly greater maximum replaces the running one and a tie keeps it
+__device__ __forceinline__ void gseg_add(GSeg& s, const GItem& it, const uint4 (&r)[4], int bf16,
+                                         int pe, int lane) {
+  float m;
+  int idx, bad;
+  piece_argmax(r, bf16, lane, m, idx, bad);
+  if (m > s.m) {
+    s.m = m;
+    s.idx = it.k * pe + idx;
+  }
+  s.bad |= bad;
+}
+
+__global__ void __launch_bounds__(kGThreads, 1) greedy_stats_kernel(const __grid_constant__ DenseParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  // a programmatic dependent of whatever precedes it on the stream: nothing
+  // is read before that grid has completed (it may have written the logits)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
+  const long long W = (long long)P.B * (G + 1) * np;
+  const long long nwt = (long long)gridDim.x * kGWarps;
+  const long long gw = (long long)blockIdx.x * kGWarps + warp;
+  const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (lo >= hi) return;
+  const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
+  GSeg seg;
+  GItem out = gitem_at(lo, G, np);
+  gseg_begin(seg, out, lo);
+
+  if (!P.aligned) {  // rows not 16-byte aligned: plain loads, no ring
+    for (long long w = lo; w < hi; ++w, gitem_next(out, G, np)) {
+      if (out.b != seg.b || out.j != seg.j) {
+        gseg_write(P, seg, lane);
+        gseg_begin(seg, out, w);
+      }
+      const int ne = min(pe, P.V - out.k * pe);
+      uint4 r[4];
+      load_vectors(target_row(P, out.b, out.j) + (size_t)out.k * kPieceBytes, ne, P.bf16, 0, lane, r);
+      gseg_add(seg, out, r, P.bf16, pe, lane);
+    }
+    gseg_write(P, seg, lane);
+    return;
+  }
+
+  unsigned char* ring = smem_raw + (size_t)warp * kGStages * kPieceBytes;
+  GItem in = out;
+  long long wi = lo;
+  auto issue = [&](int s) {
+    const int ne = min(pe, P.V - in.k * pe);
+    const unsigned char* src = target_row(P, in.b, in.j) + (size_t)in.k * kPieceBytes;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      if (vi * epv < ne) cp_async16(ring + s * kPieceBytes + 16 * vi, src + 16 * vi);
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < kGStages - 1; ++s) {
+    if (wi < hi) {
+      issue(s);
+      gitem_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+  }
+  int slot = 0, islot = kGStages - 1;
+  for (long long w = lo; w < hi; ++w) {
+    if (out.b != seg.b || out.j != seg.j) {
+      gseg_write(P, seg, lane);
+      gseg_begin(seg, out, w);
+    }
+    if (wi < hi) {
+      issue(islot);
+      gitem_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+    cp_async_wait_group<kGStages - 1>();
+    const unsigned char* stage = ring + slot * kPieceBytes;
+    const int ne = min(pe, P.V - out.k * pe);
+    uint4 r[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      r[i] = (vi * epv < ne) ? *reinterpret_cast<const uint4*>(stage + 16 * vi)
+                             : make_uint4(ninf, ninf, ninf, ninf);
+    }
+    gseg_add(seg, out, r, P.bf16, pe, lane);
+    gitem_next(out, G, np);
+    slot = (slot + 1 == kGStages) ? 0 : slot + 1;
+    islot = (islot + 1 == kGStages) ? 0 : islot + 1;
+  }
+  gseg_write(P, seg, lane);
+  cp_async_wait_group<0>();
+}
+
+// Row b: a warp per position combines the position's records into a_j, then
+// the first mismatch and the tokens.  Clears the records it read.
+__global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __grid_constant__ DenseParams P) {
+  __shared__ int s_n, s_err;
+  __shared__ int s_arg[kGMaxPos];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x, G = P.G, np = P.g.np;
+  if (threadIdx.x == 0) {
+    s_n = G;
+    s_err = 0;
+  }
+  // the statistics grid's records must be complete and visible
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  ArgRec* rec = reinterpret_cast<ArgRec*>(P.ws + P.L.upart);
+  // the statistics grid gave warp g the pieces [lo(g), lo(g + 1)), lo(g) =
+  // g W / nwt; a segment record sits at the first piece of each segment
+  const long long W = (long long)P.B * (G + 1) * np, nwt = P.stats_warps;
+  for (int j = warp; j <= G; j += kGRowWarps) {
+    const int xj = (j < G) ? P.x[(size_t)b * G + j] : 0;
+    const long long P0 = ((long long)b * (G + 1) + j) * np, P1 = P0 + np;
+    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    float m = -INFINITY;
+    int idx = INT_MAX, bad = 0;
+    for (long long g = g0 + lane; g <= g1; g += 32) {
+      const long long l0 = g * W / nwt, l1 = (g + 1) * W / nwt;
+      if (l1 <= l0) continue;  // an empty range writes nothing
+      int4* rp = reinterpret_cast<int4*>(rec + (l0 > P0 ? l0 : P0));
+      const int4 v = __ldcg(rp);
+      *rp = make_int4(0, 0, 0, 0);
+      const float rm = __int_as_float(v.x);
+      if (rm > m || (rm == m && v.y < idx)) {
+        m = rm;
+        idx = v.y;
+      }
+      bad |= v.z;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float om = __shfl_xor_sync(0xffffffffu, m, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      if (om > m || (om == m && oi < idx)) {
+        m = om;
+        idx = oi;
+      }
+    }
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      const int err = bad || !(m > -INFINITY) || (j < G && (xj < 0 || xj >= P.V));
+      s_arg[j] = idx;
+      if (err) atomicOr(&s_err, 1);
+      else if (j < G && xj != idx) atomicMin(&s_n, j);
+    }
+  }
+  __syncthreads();
+  const int err = s_err, n = s_n;
+  int32_t* tok = P.tok_out + (size_t)b * (G + 1);
+  for (int j = threadIdx.x; j <= G; j += blockDim.x) {
+    int v = -1;
+    if (!err) v = (j < n) ? P.x[(size_t)b * G + j] : (j == n ? s_arg[n] : -1);
+    tok[j] = v;
+  }
+  if (threadIdx.x == 0) {
+    P.n_out[b] = err ? -1 : n;
+    if (err) atomicOr(&reinterpret_cast<WsHeader*>(P.ws)->status, kStatusInputErr);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s) {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {  // once per device: SM count and the ring's shared memory
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(greedy_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGSmem);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n;
+  }
+  const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
+  long long grid = sms[dev];
+  if (grid * kGWarps > pieces) grid = (pieces + kGWarps - 1) / kGWarps;
+  DenseParams q = p;
+  q.stats_warps = grid * kGWarps;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t k1 = {};
+  k1.gridDim = dim3((unsigned)grid, 1, 1);
+  k1.blockDim = dim3(kGThreads, 1, 1);
+  k1.dynamicSmemBytes = kGSmem;
+  k1.stream = s;
+  k1.attrs = attr;
+  k1.numAttrs = 1;
+  e = cudaLaunchKernelEx(&k1, greedy_stats_kernel, q);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t k2 = {};
+  k2.gridDim = dim3((unsigned)p.B, 1, 1);
+  k2.blockDim = dim3(32 * kGRowWarps, 1, 1);
+  k2.stream = s;
+  k2.attrs = attr;
+  k2.numAttrs = 1;
+  return cudaLaunchKernelEx(&k2, greedy_row_kernel, q);
+}
+
+}  // namespace sv

@@ -153,6 +153,7 @@ struct SparseParams {
 // the two dense kernels (statistics + row decisions, then residual + draw)
 cudaError_t launch_dense(const DenseParams& p, cudaStream_t s);
 cudaError_t launch_dense_resid_out(const DenseParams& p, float* resid_out, cudaStream_t s);
+cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s);  // greedy: target logits and ids only
 cudaError_t launch_small(const SmallParams& p, cudaStream_t s);
 size_t small_smem_per_warp(int R, int vstride);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);

@@ -29,6 +29,9 @@ Workloads (sizes and distributions of the five verification workloads):
 ``anyorder_b4096_w32_v33`` B=4096, D=W=32, V=33, fp32; draft ~ N(0, 2^2),
                            target = draft + N(0, 0.4^2); sigma a random
                            permutation per sequence.
+``greedy_b64_g7_v128256``  greedy (T = 0) verification on the headline shape:
+                           B=64, gamma=7, V=128256, bf16 target ~ N(0, 3^2);
+                           draft ids = argmax of target + N(0, 0.5^2).
 =========================  ===================================================
 """
 from __future__ import annotations
@@ -273,6 +276,8 @@ WORKLOADS = {
                                  target_sigma=3.0, draft_noise=0.5),
     "sparse_b256_g15_k64": dict(kind="sparse", B=256, gamma=15, V=151936, k=64),
     "anyorder_b4096_w32_v33": dict(kind="anyorder", B=4096, D=32, W=32, V=33, dtype="f32"),
+    "greedy_b64_g7_v128256": dict(kind="greedy", B=64, gamma=7, V=128256, dtype="bf16",
+                                  target_sigma=3.0, draft_noise=0.5),
 }
 
 
@@ -287,6 +292,9 @@ def make(name: str, seed: int = 0, **override) -> dict:
     elif kind == "sparse":
         B, g, V = cfg.pop("B"), cfg.pop("gamma"), cfg.pop("V")
         d = sparse_inputs(B, g, V, seed=seed, **cfg)
+    elif kind == "greedy":
+        B, g, V = cfg.pop("B"), cfg.pop("gamma"), cfg.pop("V")
+        d = greedy_inputs(B, g, V, seed=seed, **cfg)
     else:
         B, D, W, V = cfg.pop("B"), cfg.pop("D"), cfg.pop("W"), cfg.pop("V")
         d = anyorder_inputs(B, D, W, V, seed=seed, **cfg)
