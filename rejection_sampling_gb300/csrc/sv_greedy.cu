@@ -97,54 +97,63 @@ __device__ __forceinline__ void load_vectors(const unsigned char* base, int ne, 
   }
 }
 
-// (max, first index of the max, bad) of a piece, on every lane.  Element
-// e of vector vi is id vi * epv + e of the piece; a lane visits its ids in
-// increasing order and keeps the first maximum, the warp keeps the smallest
-// id among equal maxima.  NaN never compares greater, so it is never chosen;
-// it (and +inf) marks the piece bad.
+// maxima that propagate NaN (max.NaN): a NaN anywhere makes the result NaN
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float d;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
+// (max, first index of the max, bad) of a piece, on every lane.  Element e
+// of vector vi is id vi * epv + e of the piece.  The maximum comes first, by
+// packed maxima that propagate NaN; then only the lanes holding it look for
+// its first id among their elements, and the warp keeps the smallest.  The
+// piece is bad when the maximum is NaN (a NaN anywhere) or +inf.
 __device__ __forceinline__ void piece_argmax(const uint4 (&r)[4], int bf16, int lane, float& m,
                                              int& idx, int& bad) {
-  const int epv = bf16 ? 8 : 4;
-  float bv = -INFINITY;
-  int bi = INT_MAX, bd = 0;
+  float lm;
+  if (bf16) {
+    uint32_t mx = kNegInf2;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
-    const int id0 = (lane + 32 * i) * epv;
-    if (bf16) {
+    for (int i = 0; i < 4; ++i)
+      mx = bf16x2_max_nan(mx, bf16x2_max_nan(bf16x2_max_nan(r[i].x, r[i].y),
+                                             bf16x2_max_nan(r[i].z, r[i].w)));
+    lm = fmax_nan(bf16_lo(mx), bf16_hi(mx));
+  } else {
+    lm = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float v = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
-        bd |= (v != v) || (v == INFINITY);
-        if (v > bv) {
-          bv = v;
-          bi = id0 + e;
-        }
-      }
-    } else {
+    for (int i = 0; i < 4; ++i)
+      lm = fmax_nan(lm, fmax_nan(fmax_nan(__uint_as_float(r[i].x), __uint_as_float(r[i].y)),
+                                 fmax_nan(__uint_as_float(r[i].z), __uint_as_float(r[i].w))));
+  }
+  float wm = lm;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float v = __uint_as_float(w[e]);
-        bd |= (v != v) || (v == INFINITY);
-        if (v > bv) {
-          bv = v;
-          bi = id0 + e;
-        }
+  for (int o = 16; o > 0; o >>= 1) wm = fmax_nan(wm, __shfl_xor_sync(0xffffffffu, wm, o));
+  bad = (wm != wm) || (wm == INFINITY);
+  int bi = INT_MAX;
+  if (!bad && lm == wm) {  // this lane holds the maximum: its first id with it
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {  // scanned backwards, so the last hit is the first id
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+      if (bf16) {
+#pragma unroll
+        for (int e = 7; e >= 0; --e)
+          if (((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) == wm) bi = (lane + 32 * i) * 8 + e;
+      } else {
+#pragma unroll
+        for (int e = 3; e >= 0; --e)
+          if (__uint_as_float(w[e]) == wm) bi = (lane + 32 * i) * 4 + e;
       }
     }
   }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-    if (ov > bv || (ov == bv && oi < bi)) {
-      bv = ov;
-      bi = oi;
-    }
-  }
-  m = bv;
+  bi = (int)__reduce_min_sync(0xffffffffu, (unsigned)bi);
+  m = wm;
   idx = bi;
-  bad = __any_sync(0xffffffffu, bd);
 }
 
 struct GItem {  // piece k of row-position (b, j)
