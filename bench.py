@@ -502,23 +502,31 @@ def run_reference(args):
 
 
 def run_calls_only(args):
-    """Profiling driver: the headline workload through spec_verify_dense,
-    args.calls_only times, no timing and no output beyond one status line
-    (ncu's launch filters pick the kernels out)."""
-    import numpy as np
+    """Profiling driver: args.calls_only untimed calls of one workload (the
+    headline by default; ``--workload greedy_b64_g7_v128256`` for the greedy
+    path), no output beyond one status line (ncu's launch filters pick the
+    kernels out)."""
     import torch
     import rejection_sampling_gb300 as rs
     from rejection_sampling_gb300 import workloads as wl
     rs.build()
     rs.load()
     dev = torch.device("cuda", torch.cuda.current_device())
-    d = wl.make(WORKLOAD, seed=args.seed)
-    t = [to_dev(d[k], dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
+    name = args.workload or WORKLOAD
+    d = wl.make(name, seed=args.seed)
+    if d["kind"] == "greedy":
+        t = [to_dev(d[k], dev) for k in ("target", "draft_ids")]
+        fn = rs.spec_verify_greedy
+    elif d["kind"] == "dense":
+        t = [to_dev(d[k], dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
+        fn = rs.spec_verify_dense
+    else:
+        raise SystemExit(f"--calls-only drives dense and greedy workloads, not {name}")
     for _ in range(args.calls_only):
-        rs.spec_verify_dense(*t)
+        fn(*t)
     torch.cuda.synchronize()
     rc = rs.check(dev, torch.cuda.current_stream(dev))
-    print(f"{args.calls_only} calls of {WORKLOAD}: {rs.status_string(rc)}")
+    print(f"{args.calls_only} calls of {name}: {rs.status_string(rc)}")
     if rc != rs.SV_OK:
         raise SystemExit(1)
 
@@ -537,6 +545,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", dest="no_cpu_baseline", action="store_true")
     ap.add_argument("--calls-only", dest="calls_only", type=int, default=0,
                     help="profiling driver: N untimed calls on the headline workload")
+    ap.add_argument("--workload", default=None,
+                    help="with --calls-only: the workload to drive (default: the headline)")
     args = ap.parse_args(argv)
     if args.calls_only > 0:
         run_calls_only(args)
