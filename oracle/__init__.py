@@ -61,8 +61,9 @@ def _load():
             lib.oracle_verify_sparse.argtypes = [P, P, I, P, P, I, P, P, P, I, I, I, P, P, P, P, P, P, I]
             lib.oracle_verify_anyorder.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, P, P, P, P, P, I]
             lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, I]
+            lib.oracle_commit_confident.argtypes = [P, I, P, ctypes.c_double, I, I, I, P, P, P, P, I]
             for f in (lib.oracle_verify_dense, lib.oracle_verify_sparse, lib.oracle_verify_anyorder,
-                      lib.oracle_verify_greedy):
+                      lib.oracle_verify_greedy, lib.oracle_commit_confident):
                 f.restype = I
             lib.oracle_default_threads.restype = I
             _lib = lib
@@ -132,6 +133,23 @@ def verify_greedy(target, draft_ids, *, nthreads: int = 0) -> dict:
                                   _ptr(out["out_tokens"]), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_verify_greedy failed")
+    return out
+
+
+def commit_confident(logits, masked, tau: float, *, nthreads: int = 0) -> dict:
+    """Confidence-threshold commit of B blocks ("SDAR" page, section 5).
+    logits [B, W, V]; masked [B, W] (nonzero: still masked)."""
+    lib = _load()
+    lt, dt = _logits(logits)
+    B, W, V = lt.shape
+    m = np.ascontiguousarray(masked, dtype=np.int32).reshape(B, W)
+    out = dict(commit=np.zeros((B, W), np.int32), tokens=np.zeros((B, W), np.int32),
+               confidence=np.zeros((B, W), np.float64), flags=np.zeros(B, np.uint32))
+    rc = lib.oracle_commit_confident(_ptr(lt), dt, _ptr(m), float(tau), B, W, V,
+                                     _ptr(out["commit"]), _ptr(out["tokens"]),
+                                     _ptr(out["confidence"]), _ptr(out["flags"]), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_commit_confident failed")
     return out
 
 

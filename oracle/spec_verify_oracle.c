@@ -21,6 +21,10 @@
  *  [DF4g] same guide, 4.4: under greedy decoding (T = 0) a draft token is
  *         accepted if and only if a condition holds whose formula did not
  *         survive on the page (see oracle_verify_greedy for the reading).
+ *  [SDAR] "SDAR" page, section 5 (decoding timeline): each pass gives a full
+ *         distribution at every masked position of the block; positions
+ *         whose confidence clears a threshold tau are committed, at least
+ *         the most confident one, so progress is guaranteed.
  *  [SSMD] "Self-Speculative Masked Diffusions", key design 2: verification
  *         in sigma order from the first unknown position; at the first
  *         rejection resample from max(0, target - draft) and end the round.
@@ -617,4 +621,96 @@ int oracle_verify_greedy(const void* target_logits, int dtype, const int32_t* dr
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
   greedy_args a = {target_logits, dtype, draft_ids, B, gamma, V, n_accepted, out_tokens};
   return run_rows(greedy_row, &a, B, 1, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Confidence-threshold commit [SDAR]                                   */
+/* ------------------------------------------------------------------ */
+/* Readings (the page states the rule in prose only): the confidence of a
+ * masked position is its largest probability, max_y p_i(y) = 1 / sum_y
+ * exp(l_y - max l); its candidate token is the argmax (smallest id on ties);
+ * "clears tau" is conf > tau; "at least the argmax is" committed means that
+ * when no masked position clears tau, the one with the largest confidence
+ * (the smallest index on ties) is committed. */
+typedef struct {
+  const void* lt;
+  int dtype;
+  const int32_t* masked;
+  double tau;
+  int B, W, V;
+  int32_t *commit, *tokens;
+  double* conf;
+  uint32_t* flags;
+} commit_args;
+
+static void commit_row(const void* pa, int b, double* p) {
+  const commit_args* a = (const commit_args*)pa;
+  const int W = a->W, V = a->V;
+  int32_t* cm = a->commit + (size_t)b * W;
+  int32_t* tk = a->tokens + (size_t)b * W;
+  double* cf = a->conf ? a->conf + (size_t)b * W : NULL;
+  uint32_t flag = 0;
+  int bad = 0;
+  for (int i = 0; i < W && !bad; ++i)
+    if (a->masked[(size_t)b * W + i])
+      bad |= check_row(a->lt, a->dtype, ((size_t)b * W + i) * (size_t)V, V);
+  if (bad) {
+    for (int i = 0; i < W; ++i) {
+      cm[i] = -1;
+      tk[i] = -1;
+      if (cf) cf[i] = NAN;
+    }
+    if (a->flags) a->flags[b] = ORACLE_FLAG_INPUT_ERR;
+    return;
+  }
+  int ncommit = 0, best = -1;
+  double best_c = -1.0, second_c = -1.0;
+  for (int i = 0; i < W; ++i) {
+    cm[i] = 0;
+    tk[i] = -1;
+    if (cf) cf[i] = NAN;
+    if (!a->masked[(size_t)b * W + i]) continue;
+    const size_t off = ((size_t)b * W + i) * (size_t)V;
+    softmax_row(a->lt, a->dtype, off, V, p);
+    int y = 0;
+    for (int v = 1; v < V; ++v)
+      if (p[v] > p[y]) y = v;
+    const double c = p[y];
+    if (cf) cf[i] = c;
+    if (fabs(c - a->tau) < ORACLE_ACCEPT_BAND) flag |= ORACLE_FLAG_ACCEPT_BAND;
+    if (c > a->tau) {
+      cm[i] = 1;
+      tk[i] = y;
+      ++ncommit;
+    }
+    if (c > best_c) {
+      second_c = best_c;
+      best_c = c;
+      best = i;
+    } else if (c > second_c) {
+      second_c = c;
+    }
+  }
+  if (ncommit == 0 && best >= 0) {  /* progress: the most confident position */
+    const size_t off = ((size_t)b * W + best) * (size_t)V;
+    softmax_row(a->lt, a->dtype, off, V, p);
+    int y = 0;
+    for (int v = 1; v < V; ++v)
+      if (p[v] > p[y]) y = v;
+    cm[best] = 1;
+    tk[best] = y;
+    if (second_c >= 0.0 && best_c - second_c <= ORACLE_TIE_BAND * best_c) flag |= ORACLE_FLAG_CDF_TIE;
+  }
+  if (a->flags) a->flags[b] = flag;
+}
+
+int oracle_commit_confident(const void* logits, int dtype, const int32_t* masked, double tau,
+                            int B, int W, int V, int32_t* commit, int32_t* tokens,
+                            double* confidence, uint32_t* flags, int nthreads) {
+  if (B < 0 || W <= 0 || V <= 0) return -1;
+  if (B == 0) return 0;
+  if (!logits || !masked || !commit || !tokens) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  commit_args a = {logits, dtype, masked, tau, B, W, V, commit, tokens, confidence, flags};
+  return run_rows(commit_row, &a, B, (size_t)V, nthreads);
 }

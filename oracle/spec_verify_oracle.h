@@ -113,6 +113,27 @@ int oracle_verify_greedy(const void* target_logits, int dtype, const int32_t* dr
                          int gamma, int V, int32_t* n_accepted, int32_t* out_tokens,
                          int nthreads);
 
+/* Confidence-threshold commit of a block-diffusion pass ("SDAR" page,
+ * section 5, decoding timeline): every masked position of a block has a full
+ * distribution p_i = softmax(logits[b, i]); its confidence is max_y p_i(y)
+ * and its candidate token the argmax (the smallest id on ties).  Masked
+ * positions whose confidence clears tau (conf > tau) are committed; if none
+ * does, the single most confident masked position is (the smallest index on
+ * ties), so every pass makes progress.
+ *   logits [B, W, V] (dtype); masked [B, W] int32 (nonzero: still masked);
+ *   commit [B, W] int32 (1 committed, 0 not, -1 on an input error in the
+ *   block); tokens [B, W] int32 (the argmax where committed, else -1);
+ *   confidence [B, W] or NULL (NaN where not masked); flags [B] or NULL:
+ *   ORACLE_FLAG_ACCEPT_BAND when a masked position's confidence is within
+ *   1e-6 of tau, ORACLE_FLAG_CDF_TIE when the fallback's top two confidences
+ *   are within 1e-6 relative, ORACLE_FLAG_INPUT_ERR on an input error (a
+ *   masked row with NaN, +inf or no finite logit).  A block with no masked
+ *   position commits nothing.
+ */
+int oracle_commit_confident(const void* logits, int dtype, const int32_t* masked, double tau,
+                            int B, int W, int V, int32_t* commit, int32_t* tokens,
+                            double* confidence, uint32_t* flags, int nthreads);
+
 /* Threads the oracle would use for nthreads <= 0 (all online host cores). */
 int oracle_default_threads(void);
 

@@ -39,7 +39,7 @@ from __future__ import annotations
 import numpy as np
 
 __all__ = [
-    "bf16_bits", "bf16_bits_to_f32", "gumbel_argmax", "dense_inputs", "greedy_inputs",
+    "bf16_bits", "bf16_bits_to_f32", "gumbel_argmax", "dense_inputs", "greedy_inputs", "commit_inputs",
     "sparse_inputs", "anyorder_inputs", "WORKLOADS", "make",
 ]
 
@@ -170,6 +170,32 @@ def greedy_inputs(B: int, gamma: int, V: int, *, dtype: str = "bf16", seed: int 
     draft_ids = np.argmax(_as_f64(ld_q), axis=-1).astype(np.int32) if gamma else np.zeros((B, 0), np.int32)
     return dict(kind="greedy", dtype=dtype, B=B, gamma=gamma, V=V,
                 target=np.ascontiguousarray(lt_q), draft_ids=np.ascontiguousarray(draft_ids))
+
+
+def commit_inputs(B: int, W: int, V: int, *, dtype: str = "bf16", seed: int = 0,
+                  sigma: float = 3.0, spike_lo: float = 10.0, spike_hi: float = 40.0,
+                  masked_frac: float = 0.75, tau: float = 0.9) -> dict:
+    """Confidence-threshold commit inputs: B blocks of W positions.
+
+    logits [B, W, V] ~ N(0, sigma^2) plus one spike per position at a random
+    id, its height uniform in [spike_lo, spike_hi] (so the positions' largest
+    probabilities spread over (0, 1)); masked [B, W] int32, each position still
+    masked with probability masked_frac; threshold tau.
+    """
+    rng = np.random.default_rng(seed)
+    lt = rng.normal(0.0, sigma, size=(B, W, V)).astype(np.float32)
+    ids = rng.integers(0, V, size=(B, W))
+    h = rng.uniform(spike_lo, spike_hi, size=(B, W)).astype(np.float32)
+    np.put_along_axis(lt, ids[..., None], np.take_along_axis(lt, ids[..., None], -1) + h[..., None], -1)
+    if dtype == "bf16":
+        lq = bf16_bits(lt)
+    elif dtype == "f32":
+        lq = lt
+    else:
+        raise ValueError(dtype)
+    masked = (rng.random((B, W)) < masked_frac).astype(np.int32)
+    return dict(kind="commit", dtype=dtype, B=B, W=W, V=V, tau=float(tau),
+                logits=np.ascontiguousarray(lq), masked=masked)
 
 
 # ---------------------------------------------------------------------------
