@@ -215,7 +215,7 @@ def variant_lines(dev, stream):
     from rejection_sampling_gb300 import workloads as wl
     out = {}
     for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33",
-                 "greedy_b64_g7_v128256"):
+                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936"):
         d = wl.make(name, seed=0)
         copies = 8  # rotate over copies so the inputs exceed L2 where they are small
         calls = []
@@ -241,6 +241,18 @@ def variant_lines(dev, stream):
                 o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
                 calls.append(rs.prepare_greedy(*args, out=o, stream=stream))
+        elif d["kind"] == "commit":
+            B, W, V = d["B"], d["W"], d["V"]
+            nmask = int(np.count_nonzero(d["masked"]))
+            nbytes = nmask * V * (2 if d["dtype"] == "bf16" else 4)  # masked positions' logits
+            positions = nmask
+            copies = 4  # 4 x 78 MB > L2
+            base = [to_dev(d[k], dev) for k in ("logits", "masked")]
+            for c in range(copies):
+                args = [t.clone() for t in base]
+                o = rs.CommitResult(torch.empty(B, W, dtype=torch.int32, device=dev),
+                                    torch.empty(B, W, dtype=torch.int32, device=dev), None)
+                calls.append(rs.prepare_commit(*args, d["tau"], out=o, stream=stream))
         elif d["kind"] == "sparse":
             B, G, k = d["B"], d["gamma"], d["kt"]
             nbytes = B * ((G + 1) * k + G * k) * 8 + B * G * 8 + B * 4
@@ -268,7 +280,7 @@ def variant_lines(dev, stream):
                      "positions_per_s": positions / (ms * 1e-3),
                      "GBps": nbytes / (ms * 1e-3) / 1e9,
                      "bytes_per_call": nbytes}
-        if d["kind"] == "greedy":  # a streaming pass over the target logits: HBM roofline
+        if d["kind"] in ("greedy", "commit"):  # streaming passes over logits: HBM roofline
             peak, _ = measured_peak()
             out[name]["frac_of_measured_hbm"] = out[name]["GBps"] / peak
         del calls
@@ -520,8 +532,11 @@ def run_calls_only(args):
     elif d["kind"] == "dense":
         t = [to_dev(d[k], dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
         fn = rs.spec_verify_dense
+    elif d["kind"] == "commit":
+        t = [to_dev(d[k], dev) for k in ("logits", "masked")] + [d["tau"]]
+        fn = rs.spec_commit_confident
     else:
-        raise SystemExit(f"--calls-only drives dense and greedy workloads, not {name}")
+        raise SystemExit(f"--calls-only drives dense, greedy and commit workloads, not {name}")
     for _ in range(args.calls_only):
         fn(*t)
     torch.cuda.synchronize()

@@ -200,6 +200,29 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, const int32_t*
                        void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /*
+ * spec_commit_confident -- confidence-threshold commit of one block-diffusion
+ * pass ("SDAR" page, section 5, decoding timeline: positions whose
+ * confidence clears a threshold tau are committed, at least the most
+ * confident one, so every pass makes progress).  For every position i still
+ * masked in block b: confidence c_i = the largest probability of
+ * softmax(logits[b, i]) and token a_i = its argmax (the smallest id on ties).
+ * Masked positions with c_i > tau are committed; if none is, the most
+ * confident masked position is (the smallest index on ties).
+ *   logits [B, W, V] (fp32 or bf16); masked [B, W] int32 (nonzero: still
+ *   masked; the logits of other positions are not read); tau: threshold.
+ * Outputs: commit [B, W] int32 (1 committed, 0 not, -1 in a block with an
+ *   input error: a masked row with NaN, +inf or no finite logit);
+ *   tokens [B, W] int32 (a_i where committed, else -1); confidence [B, W]
+ *   fp32 or NULL (c_i; NaN where not masked or on an input error).
+ * Workspace: spec_verify_workspace_size(B, W - 1, V) bytes, zero again after
+ * the call.  Limits: W <= 256, V <= SV_MAX_VOCAB.
+ */
+int spec_commit_confident(const void* logits, sv_dtype dtype, const int32_t* masked, float tau,
+                          int B, int W, int V, int32_t* commit, int32_t* tokens,
+                          float* confidence, void* workspace, size_t ws_bytes,
+                          sv_stream_t stream);
+
+/*
  * spec_verify_check -- synchronise `stream`, read and clear the workspace
  * status word.  Returns SV_OK, SV_ERR_DEVICE_INPUT (some row of an earlier
  * call had invalid inputs; those rows carry n_accepted = -1),

@@ -27,6 +27,7 @@ EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
     "spec_verify_status_string", "spec_verify_dense_static", "spec_verify_greedy",
+    "spec_commit_confident",
 )
 
 
@@ -76,6 +77,8 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_status_string.argtypes = [I]
         lib.spec_verify_greedy.restype = I
         lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
+        lib.spec_commit_confident.restype = I
+        lib.spec_commit_confident.argtypes = [P, I, P, ctypes.c_float, I, I, I, P, P, P, P, Z, P]
         lib.spec_verify_dense_static.restype = I
         lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         _lib = lib
@@ -228,6 +231,55 @@ def spec_verify_greedy(target_logits: torch.Tensor, draft_ids: torch.Tensor, *,
     if rc != SV_OK:
         raise SpecVerifyError(rc, "spec_verify_greedy")
     return out
+
+
+class CommitResult(NamedTuple):
+    commit: torch.Tensor
+    tokens: torch.Tensor
+    confidence: Optional[torch.Tensor]
+
+
+def spec_commit_confident(logits: torch.Tensor, masked: torch.Tensor, tau: float, *,
+                          confidence: bool = False, out: Optional[CommitResult] = None,
+                          stream: Optional[torch.cuda.Stream] = None) -> CommitResult:
+    """Confidence-threshold commit of B blocks.  logits [B, W, V] (bf16 or fp32,
+    CUDA), masked [B, W] int32 (nonzero: still masked), threshold tau."""
+    lib = load()
+    dev = logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_commit_confident needs CUDA tensors")
+    dt = _logit_dtype(logits)
+    B, W, V = logits.shape
+    _req(logits, "logits", logits.dtype, (B, W, V), dev)
+    _req(masked, "masked", torch.int32, (B, W), dev)
+    if out is None:
+        out = CommitResult(torch.empty(B, W, dtype=torch.int32, device=dev),
+                           torch.empty(B, W, dtype=torch.int32, device=dev),
+                           torch.empty(B, W, dtype=torch.float32, device=dev) if confidence else None)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, W - 1, V), dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_commit_confident(_ptr(logits), dt, _ptr(masked), float(tau), B, W, V,
+                                       _ptr(out.commit), _ptr(out.tokens), _ptr(out.confidence),
+                                       ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_commit_confident")
+    return out
+
+
+def prepare_commit(logits, masked, tau: float, out: CommitResult,
+                   stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """Validate once and return a PreparedCall repeating spec_commit_confident."""
+    spec_commit_confident(logits, masked, tau, out=out, stream=stream)
+    lib = load()
+    dev = logits.device
+    B, W, V = logits.shape
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(workspace_size(B, W - 1, V), dev, sp)
+    args = (_ptr(logits), _logit_dtype(logits), _ptr(masked), ctypes.c_float(float(tau)), B, W, V,
+            _ptr(out.commit), _ptr(out.tokens), _ptr(out.confidence), ws.data_ptr(), ws.numel(), sp)
+    keep = (logits, masked, out, ws)
+    return PreparedCall(lib.spec_commit_confident, args, keep, "spec_commit_confident")
 
 
 def prepare_greedy(target_logits, draft_ids, out: VerifyResult,

@@ -157,6 +157,40 @@ int spec_verify_greedy(const void* target_logits, sv_dtype dtype, const int32_t*
   return launch_status(sv::launch_greedy(p, (cudaStream_t)stream));
 }
 
+int spec_commit_confident(const void* logits, sv_dtype dtype, const int32_t* masked, float tau,
+                          int B, int W, int V, int32_t* commit, int32_t* tokens,
+                          float* confidence, void* workspace, size_t ws_bytes,
+                          sv_stream_t stream) {
+  if (B < 0 || W < 1 || W > SV_MAX_GAMMA + 1 || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (tau != tau) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !masked || !commit || !tokens || !workspace) return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(logits, es) || !aligned_to(masked, 4) || !aligned_to(commit, 4) ||
+      !aligned_to(tokens, 4) || (confidence && !aligned_to(confidence, 4)) ||
+      !aligned_to(workspace, 256))
+    return SV_ERR_INVALID_ARG;
+  const sv::DenseGeom g = sv::dense_geom(V, es);
+  const sv::DenseLayout L = sv::dense_layout(B, W - 1, g);
+  if (ws_bytes < L.total) return SV_ERR_INVALID_ARG;
+  if ((long long)B * W * g.np >= (1ll << 31) - 1) return SV_ERR_INVALID_ARG;
+  sv::DenseParams p;
+  memset(&p, 0, sizeof p);
+  p.lt = static_cast<const unsigned char*>(logits);
+  p.x = masked;
+  p.tok_out = tokens;
+  p.ws = static_cast<unsigned char*>(workspace);
+  p.L = L;
+  p.g = g;
+  p.B = B;
+  p.G = W - 1;
+  p.V = V;
+  p.bf16 = (dtype == SV_BF16);
+  p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(logits, 16);
+  return launch_status(sv::launch_commit(p, tau, commit, confidence, (cudaStream_t)stream));
+}
+
 int spec_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,
                        const int32_t* drf_ids, const float* drf_probs, int kd,
                        const int32_t* draft_tokens, const float* u_accept, const float* u_sample,

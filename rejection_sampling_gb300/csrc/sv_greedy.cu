@@ -364,7 +364,314 @@ __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __gri
   }
 }
 
+// ---------------------------------------------------------------------------
+// Confidence-threshold commit of a block-diffusion pass ("SDAR" page,
+// section 5, decoding timeline).  For every masked position i of block b:
+// confidence c_i = max_y p_i(y) = 1 / S_i, S_i = sum_y 2^((l_y - max l) log2e),
+// token a_i = argmax (smallest id on ties); masked positions with c_i > tau
+// are committed, and when none clears tau the most confident one is (the
+// smallest index on ties), so every pass makes progress.
+//  * commit_stats_kernel: the greedy statistics kernel's sweep over the
+//    logits [B, W, V] (pieces of positions no longer masked are skipped),
+//    adding per piece S = sum 2^((v - m) log2e) (ex2.approx) to (max, first
+//    id, bad); segments fold (m, S) with one rescale (float-float).
+//  * commit_row_kernel: one CTA per block; a warp per masked position
+//    combines its records into (c_i, a_i); thread 0 applies the threshold.
+// ---------------------------------------------------------------------------
+struct ConfRec {  // one segment (32 bytes, at the segment's first piece slot)
+  float m;        // maximum
+  float s_hi, s_lo;  // sum 2^((v - m) log2e), float-float
+  int idx;        // first id holding the maximum
+  int bad;        // a NaN or +inf was seen
+  int pad[3];
+};
+
+struct CSeg {
+  long long w0;
+  int b, j;
+  float m;
+  ff S;
+  int idx, bad;
+  bool live;  // the position is masked (a record will be written)
+};
+
+__device__ __forceinline__ bool is_masked(const DenseParams& P, int b, int j) {
+  return __ldg(P.x + (size_t)b * (P.G + 1) + j) != 0;
+}
+
+__device__ __forceinline__ void cseg_begin(CSeg& s, const DenseParams& P, const GItem& it, long long w) {
+  s.w0 = w;
+  s.b = it.b;
+  s.j = it.j;
+  s.m = -INFINITY;
+  s.S = ff{0.f, 0.f};
+  s.idx = INT_MAX;
+  s.bad = 0;
+  s.live = is_masked(P, it.b, it.j);
+}
+__device__ __forceinline__ void cseg_write(const DenseParams& P, const CSeg& s, int lane) {
+  if (lane == 0 && s.live) {
+    int4* q = reinterpret_cast<int4*>(reinterpret_cast<ConfRec*>(P.ws + P.L.upart) + s.w0);
+    q[0] = make_int4(__float_as_int(s.m), __float_as_int(s.S.hi), __float_as_int(s.S.lo), s.idx);
+    q[1] = make_int4(s.bad, 0, 0, 0);
+  }
+}
+// (max, sum, first id, bad) of a piece folded into the segment (pieces in
+// increasing id order: a strictly greater maximum takes over, ties keep it)
+__device__ __forceinline__ void cseg_add(CSeg& s, const GItem& it, const uint4 (&r)[4], int bf16,
+                                         int pe, int lane) {
+  float m;
+  int idx, bad;
+  piece_argmax(r, bf16, lane, m, idx, bad);
+  s.bad |= bad;
+  if (bad || m == -INFINITY) return;  // nothing to add (a bad segment is an error anyway)
+  const float c = m * kLog2e;
+  float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (bf16) {
+      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].x), kLog2e, -c));
+      a1 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].y), kLog2e, -c));
+      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].z), kLog2e, -c));
+      a1 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].w), kLog2e, -c));
+    } else {
+      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -c)) + ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -c));
+      a1 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -c)) + ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -c));
+    }
+  }
+  const float ps = warp_sum(a0 + a1);
+  if (m > s.m) {
+    s.S = ff_add(ff_mul_f(s.S, (s.m == -INFINITY) ? 0.f : ex2(s.m * kLog2e - c)), ff{ps, 0.f});
+    s.m = m;
+    s.idx = it.k * pe + idx;
+  } else {
+    s.S = ff_add(s.S, two_prod(ps, ex2(c - s.m * kLog2e)));
+  }
+}
+
+__global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid_constant__ DenseParams P) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
+  const long long W = (long long)P.B * (G + 1) * np;
+  const long long nwt = (long long)gridDim.x * kGWarps;
+  const long long gw = (long long)blockIdx.x * kGWarps + warp;
+  const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (lo >= hi) return;
+  const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
+  CSeg seg;
+  GItem out = gitem_at(lo, G, np);
+  cseg_begin(seg, P, out, lo);
+
+  if (!P.aligned) {
+    for (long long w = lo; w < hi; ++w, gitem_next(out, G, np)) {
+      if (out.b != seg.b || out.j != seg.j) {
+        cseg_write(P, seg, lane);
+        cseg_begin(seg, P, out, w);
+      }
+      if (!seg.live) continue;
+      const int ne = min(pe, P.V - out.k * pe);
+      uint4 r[4];
+      load_vectors(target_row(P, out.b, out.j) + (size_t)out.k * kPieceBytes, ne, P.bf16, 0, lane, r);
+      cseg_add(seg, out, r, P.bf16, pe, lane);
+    }
+    cseg_write(P, seg, lane);
+    return;
+  }
+
+  unsigned char* ring = smem_raw + (size_t)warp * kGStages * kPieceBytes;
+  GItem in = out;
+  long long wi = lo;
+  auto issue = [&](int s) {  // pieces of positions no longer masked are not read
+    if (!is_masked(P, in.b, in.j)) return;
+    const int ne = min(pe, P.V - in.k * pe);
+    const unsigned char* src = target_row(P, in.b, in.j) + (size_t)in.k * kPieceBytes;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int vi = lane + 32 * i;
+      if (vi * epv < ne) cp_async16(ring + s * kPieceBytes + 16 * vi, src + 16 * vi);
+    }
+  };
+#pragma unroll
+  for (int s = 0; s < kGStages - 1; ++s) {
+    if (wi < hi) {
+      issue(s);
+      gitem_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+  }
+  int slot = 0, islot = kGStages - 1;
+  for (long long w = lo; w < hi; ++w) {
+    if (out.b != seg.b || out.j != seg.j) {
+      cseg_write(P, seg, lane);
+      cseg_begin(seg, P, out, w);
+    }
+    if (wi < hi) {
+      issue(islot);
+      gitem_next(in, G, np);
+      ++wi;
+    }
+    cp_async_commit();
+    cp_async_wait_group<kGStages - 1>();
+    if (seg.live) {
+      const unsigned char* stage = ring + slot * kPieceBytes;
+      const int ne = min(pe, P.V - out.k * pe);
+      uint4 r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int vi = lane + 32 * i;
+        r[i] = (vi * epv < ne) ? *reinterpret_cast<const uint4*>(stage + 16 * vi)
+                               : make_uint4(ninf, ninf, ninf, ninf);
+      }
+      cseg_add(seg, out, r, P.bf16, pe, lane);
+    }
+    gitem_next(out, G, np);
+    slot = (slot + 1 == kGStages) ? 0 : slot + 1;
+    islot = (islot + 1 == kGStages) ? 0 : islot + 1;
+  }
+  cseg_write(P, seg, lane);
+  cp_async_wait_group<0>();
+}
+
+__global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __grid_constant__ DenseParams P,
+                                                                    float tau, int32_t* commit,
+                                                                    float* confidence) {
+  __shared__ float s_conf[kGMaxPos];
+  __shared__ int s_tok[kGMaxPos];
+  __shared__ int s_err;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = blockIdx.x, G = P.G, Wn = G + 1, np = P.g.np;
+  if (threadIdx.x == 0) s_err = 0;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __syncthreads();
+  ConfRec* rec = reinterpret_cast<ConfRec*>(P.ws + P.L.upart);
+  const long long W = (long long)P.B * Wn * np, nwt = P.stats_warps;
+  for (int j = warp; j < Wn; j += kGRowWarps) {
+    const bool masked = P.x[(size_t)b * Wn + j] != 0;
+    if (!masked) {  // no record was written for it
+      if (lane == 0) {
+        s_conf[j] = -1.f;
+        s_tok[j] = -1;
+      }
+      continue;
+    }
+    const long long P0 = ((long long)b * Wn + j) * np, P1 = P0 + np;
+    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    float m = -INFINITY;
+    ff S{0.f, 0.f};
+    int idx = INT_MAX, bad = 0;
+    for (long long g = g0 + lane; g <= g1; g += 32) {
+      const long long l0 = g * W / nwt, l1 = (g + 1) * W / nwt;
+      if (l1 <= l0) continue;
+      int4* rp = reinterpret_cast<int4*>(rec + (l0 > P0 ? l0 : P0));
+      const int4 v0 = __ldcg(rp), v1 = __ldcg(rp + 1);
+      rp[0] = make_int4(0, 0, 0, 0);
+      rp[1] = make_int4(0, 0, 0, 0);
+      bad |= v1.x;
+      const float rm = __int_as_float(v0.x);
+      const ff rs{__int_as_float(v0.y), __int_as_float(v0.z)};
+      if (rm == -INFINITY) continue;
+      if (rm > m) {
+        S = ff_add(ff_mul_f(S, (m == -INFINITY) ? 0.f : exp2f((m - rm) * kLog2e)), rs);
+        m = rm;
+        idx = v0.w;
+      } else {
+        S = ff_add(S, ff_mul_f(rs, exp2f((rm - m) * kLog2e)));
+        if (rm == m && v0.w < idx) idx = v0.w;
+      }
+    }
+    // warp: rescale every lane's sum to the warp maximum, then add
+    const float M = warp_max(m);
+    S = warp_sum_ff(ff_mul_f(S, (m == -INFINITY) ? 0.f : exp2f((m - M) * kLog2e)));
+    int ci = (m == M) ? idx : INT_MAX;
+    ci = (int)__reduce_min_sync(0xffffffffu, (unsigned)ci);
+    bad = __any_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      const float Sf = ff_to_f(S);
+      // S is at least the maximum's own term, ex2 of the rounding residual of
+      // m log2e: 1 within a few units in the last place, so 1/S can exceed 1
+      // by as much; the confidence is clamped to 1
+      const int err = bad || !(M > -INFINITY) || !(Sf > 0.f) || !(Sf < INFINITY);
+      if (err) atomicOr(&s_err, 1);
+      s_conf[j] = err ? -1.f : fminf(__fdiv_rn(1.f, Sf), 1.f);
+      s_tok[j] = ci;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const int err = s_err;
+    int32_t* cm = commit + (size_t)b * Wn;
+    int32_t* tk = P.tok_out + (size_t)b * Wn;
+    float* cf = confidence ? confidence + (size_t)b * Wn : nullptr;
+    int any = 0, best = -1;
+    float bc = -1.f;
+    for (int j = 0; j < Wn; ++j) {
+      const float c = s_conf[j];
+      const bool masked = P.x[(size_t)b * Wn + j] != 0;
+      const int on = !err && masked && c > tau;
+      cm[j] = err ? -1 : on;
+      tk[j] = on ? s_tok[j] : -1;
+      if (cf) cf[j] = (err || !masked) ? __int_as_float(0x7fc00000) : c;
+      any |= on;
+      if (masked && c > bc) {
+        bc = c;
+        best = j;
+      }
+    }
+    if (!err && !any && best >= 0) {  // progress: the most confident position
+      cm[best] = 1;
+      tk[best] = s_tok[best];
+    }
+    if (err) atomicOr(&reinterpret_cast<WsHeader*>(P.ws)->status, kStatusInputErr);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_commit(const DenseParams& p, float tau, int32_t* commit, float* confidence,
+                          cudaStream_t s) {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (sms[dev] == 0) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(commit_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kGSmem);
+    if (e != cudaSuccess) return e;
+    sms[dev] = n;
+  }
+  const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
+  long long grid = sms[dev];
+  if (grid * kGWarps > pieces) grid = (pieces + kGWarps - 1) / kGWarps;
+  DenseParams q = p;
+  q.stats_warps = grid * kGWarps;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t k1 = {};
+  k1.gridDim = dim3((unsigned)grid, 1, 1);
+  k1.blockDim = dim3(kGThreads, 1, 1);
+  k1.dynamicSmemBytes = kGSmem;
+  k1.stream = s;
+  k1.attrs = attr;
+  k1.numAttrs = 1;
+  e = cudaLaunchKernelEx(&k1, commit_stats_kernel, q);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t k2 = {};
+  k2.gridDim = dim3((unsigned)p.B, 1, 1);
+  k2.blockDim = dim3(32 * kGRowWarps, 1, 1);
+  k2.stream = s;
+  k2.attrs = attr;
+  k2.numAttrs = 1;
+  return cudaLaunchKernelEx(&k2, commit_row_kernel, q, tau, commit, confidence);
+}
 
 cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s) {
   static int sms[64] = {0};

@@ -154,6 +154,10 @@ struct SparseParams {
 cudaError_t launch_dense(const DenseParams& p, cudaStream_t s);
 cudaError_t launch_dense_resid_out(const DenseParams& p, float* resid_out, cudaStream_t s);
 cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s);  // greedy: target logits and ids only
+// confidence-threshold commit: p.lt = logits [B, W, V], p.x = masked [B, W],
+// p.G = W - 1, p.tok_out = tokens [B, W]
+cudaError_t launch_commit(const DenseParams& p, float tau, int32_t* commit, float* confidence,
+                          cudaStream_t s);
 cudaError_t launch_small(const SmallParams& p, cudaStream_t s);
 size_t small_smem_per_warp(int R, int vstride);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);

@@ -32,6 +32,11 @@ Workloads (sizes and distributions of the five verification workloads):
 ``greedy_b64_g7_v128256``  greedy (T = 0) verification on the headline shape:
                            B=64, gamma=7, V=128256, bf16 target ~ N(0, 3^2);
                            draft ids = argmax of target + N(0, 0.5^2).
+``commit_b64_w4_v151936``  confidence-threshold commit: 64 blocks of 4
+                           positions (SDAR block length), V=151936, bf16
+                           logits ~ N(0, 3^2) plus one spike of height
+                           U(10, 40) per position; 3/4 of the positions still
+                           masked; tau = 0.9.
 =========================  ===================================================
 """
 from __future__ import annotations
@@ -304,6 +309,7 @@ WORKLOADS = {
     "anyorder_b4096_w32_v33": dict(kind="anyorder", B=4096, D=32, W=32, V=33, dtype="f32"),
     "greedy_b64_g7_v128256": dict(kind="greedy", B=64, gamma=7, V=128256, dtype="bf16",
                                   target_sigma=3.0, draft_noise=0.5),
+    "commit_b64_w4_v151936": dict(kind="commit", B=64, W=4, V=151936, dtype="bf16"),
 }
 
 
@@ -321,6 +327,9 @@ def make(name: str, seed: int = 0, **override) -> dict:
     elif kind == "greedy":
         B, g, V = cfg.pop("B"), cfg.pop("gamma"), cfg.pop("V")
         d = greedy_inputs(B, g, V, seed=seed, **cfg)
+    elif kind == "commit":
+        B, W, V = cfg.pop("B"), cfg.pop("W"), cfg.pop("V")
+        d = commit_inputs(B, W, V, seed=seed, **cfg)
     else:
         B, D, W, V = cfg.pop("B"), cfg.pop("D"), cfg.pop("W"), cfg.pop("V")
         d = anyorder_inputs(B, D, W, V, seed=seed, **cfg)
