@@ -62,8 +62,10 @@ def _load():
             lib.oracle_verify_anyorder.argtypes = [P, P, I, P, P, P, P, I, I, I, I, P, P, P, P, P, P, I]
             lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, I]
             lib.oracle_commit_confident.argtypes = [P, I, P, ctypes.c_double, I, I, I, P, P, P, P, I]
+            lib.oracle_support_topk.argtypes = [P, I, I, I, ctypes.c_double, I, ctypes.c_double, P, P, P, I]
             for f in (lib.oracle_verify_dense, lib.oracle_verify_sparse, lib.oracle_verify_anyorder,
-                      lib.oracle_verify_greedy, lib.oracle_commit_confident):
+                      lib.oracle_verify_greedy, lib.oracle_commit_confident,
+                      lib.oracle_support_topk):
                 f.restype = I
             lib.oracle_default_threads.restype = I
             _lib = lib
@@ -150,6 +152,25 @@ def commit_confident(logits, masked, tau: float, *, nthreads: int = 0) -> dict:
                                      _ptr(out["confidence"]), _ptr(out["flags"]), int(nthreads))
     if rc != 0:
         raise RuntimeError("oracle_commit_confident failed")
+    return out
+
+
+def support_topk(logits, T: float, K: int, top_p: float, *, nthreads: int = 0) -> dict:
+    """Sparse support lists from dense logits [..., V]: temperature T, top-k K,
+    top-p; ids ascending [..., K], probs [..., K]."""
+    lib = _load()
+    lt, dt = _logits(logits)
+    shape = lt.shape
+    V = shape[-1]
+    N = int(np.prod(shape[:-1]))
+    out = dict(ids=np.zeros(shape[:-1] + (K,), np.int32),
+               probs=np.zeros(shape[:-1] + (K,), np.float64),
+               flags=np.zeros(shape[:-1], np.uint32))
+    rc = lib.oracle_support_topk(_ptr(lt), dt, N, V, float(T), int(K), float(top_p),
+                                 _ptr(out["ids"]), _ptr(out["probs"]), _ptr(out["flags"]),
+                                 int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_support_topk failed")
     return out
 
 

@@ -25,6 +25,9 @@
  *         distribution at every masked position of the block; positions
  *         whose confidence clears a threshold tau are committed, at least
  *         the most confident one, so progress is guaranteed.
+ *  [TKP]  Uno article (the test setting: temperature 1, top-k 50, top-p
+ *         0.95) and DFlash/DFlash2 guide, Q3 (temperature scaling of both
+ *         logit sets before the acceptance ratio; the formula is lost).
  *  [SSMD] "Self-Speculative Masked Diffusions", key design 2: verification
  *         in sigma order from the first unknown position; at the first
  *         rejection resample from max(0, target - draft) and end the round.
@@ -713,4 +716,117 @@ int oracle_commit_confident(const void* logits, int dtype, const int32_t* masked
   if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
   commit_args a = {logits, dtype, masked, tau, B, W, V, commit, tokens, confidence, flags};
   return run_rows(commit_row, &a, B, (size_t)V, nthreads);
+}
+
+/* ------------------------------------------------------------------ */
+/* Sparse support from dense logits: temperature, top-k, top-p [TKP]    */
+/* ------------------------------------------------------------------ */
+/* Readings (the usual definitions, which the pages name but do not spell
+ * out): the top-k set is the K largest logits (ties: smaller id first; the
+ * order is the same for every T > 0); its probabilities are softmax(l / T)
+ * renormalised over the set; top-p keeps, in decreasing probability (ties:
+ * smaller id first), the shortest prefix whose cumulative mass reaches top_p
+ * -- at least one entry -- and renormalises it; the other entries of the
+ * set keep their ids with probability 0, so every row is a K-entry list in
+ * ascending id order (the form the sparse verification takes). */
+typedef struct {
+  double v;
+  int32_t id;
+} vid_t;
+
+static int vid_desc(const void* a, const void* b) {
+  const vid_t* x = (const vid_t*)a;
+  const vid_t* y = (const vid_t*)b;
+  if (x->v > y->v) return -1;
+  if (x->v < y->v) return 1;
+  return (x->id > y->id) - (x->id < y->id);
+}
+
+typedef struct {
+  double p;
+  int32_t id;
+} pid_t_;
+
+static int pid_by_id(const void* a, const void* b) {
+  const pid_t_* x = (const pid_t_*)a;
+  const pid_t_* y = (const pid_t_*)b;
+  return (x->id > y->id) - (x->id < y->id);
+}
+
+typedef struct {
+  const void* lt;
+  int dtype;
+  int N, V, K;
+  double T, top_p;
+  int32_t* ids;
+  double* probs;
+  uint32_t* flags;
+} support_args;
+
+static void support_row(const void* pa, int r, double* scratch) {
+  const support_args* a = (const support_args*)pa;
+  const int V = a->V, K = a->K;
+  int32_t* oid = a->ids + (size_t)r * K;
+  double* op = a->probs + (size_t)r * K;
+  const size_t off = (size_t)r * (size_t)V;
+  if (check_row(a->lt, a->dtype, off, V)) {
+    for (int i = 0; i < K; ++i) {
+      oid[i] = -1;
+      op[i] = NAN;
+    }
+    if (a->flags) a->flags[r] = ORACLE_FLAG_INPUT_ERR;
+    return;
+  }
+  vid_t* all = (vid_t*)scratch; /* scratch holds 2V doubles: room for V pairs */
+  for (int y = 0; y < V; ++y) {
+    all[y].v = widen(a->lt, a->dtype, off + (size_t)y);
+    all[y].id = y;
+  }
+  qsort(all, (size_t)V, sizeof(vid_t), vid_desc); /* the top-k set is all[0..K) */
+  /* softmax over the set, in decreasing order (already sorted by value) */
+  const double m = all[0].v / a->T;
+  double Z = 0.0;
+  pid_t_* set = (pid_t_*)malloc(sizeof(pid_t_) * (size_t)K);
+  if (!set) return;
+  for (int i = 0; i < K; ++i) {
+    set[i].p = (all[i].v == -INFINITY) ? 0.0 : exp(all[i].v / a->T - m);
+    set[i].id = all[i].id;
+    Z += set[i].p;
+  }
+  for (int i = 0; i < K; ++i) set[i].p /= Z;
+  /* top-p: shortest prefix (decreasing probability, ties by id: the same
+   * order) with cumulative mass >= top_p, at least one entry */
+  double c = 0.0;
+  int keep = K;
+  uint32_t flag = 0;
+  for (int i = 0; i < K && a->top_p < 1.0; ++i) { /* top_p >= 1 keeps the whole set */
+    c += set[i].p;
+    if (c >= a->top_p) {
+      keep = i + 1;
+      if (c - a->top_p < ORACLE_TIE_BAND) flag |= ORACLE_FLAG_CDF_TIE;
+      break;
+    }
+    if (a->top_p - c < ORACLE_TIE_BAND) flag |= ORACLE_FLAG_CDF_TIE;
+  }
+  double Zk = 0.0;
+  for (int i = 0; i < keep; ++i) Zk += set[i].p;
+  for (int i = 0; i < K; ++i) set[i].p = (i < keep) ? set[i].p / Zk : 0.0;
+  qsort(set, (size_t)K, sizeof(pid_t_), pid_by_id);
+  for (int i = 0; i < K; ++i) {
+    oid[i] = set[i].id;
+    op[i] = set[i].p;
+  }
+  free(set);
+  if (a->flags) a->flags[r] = flag;
+}
+
+int oracle_support_topk(const void* logits, int dtype, int N, int V, double T, int K,
+                        double top_p, int32_t* ids, double* probs, uint32_t* flags,
+                        int nthreads) {
+  if (N < 0 || V <= 0 || K < 1 || K > V || !(T > 0.0)) return -1;
+  if (N == 0) return 0;
+  if (!logits || !ids || !probs) return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  support_args a = {logits, dtype, N, V, K, T, top_p, ids, probs, flags};
+  return run_rows(support_row, &a, N, 2 * (size_t)V, nthreads);
 }

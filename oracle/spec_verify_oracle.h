@@ -134,6 +134,23 @@ int oracle_commit_confident(const void* logits, int dtype, const int32_t* masked
                             int B, int W, int V, int32_t* commit, int32_t* tokens,
                             double* confidence, uint32_t* flags, int nthreads);
 
+/* Sparse support from dense logits: temperature, top-k, top-p (the Uno
+ * article's test setting, top-k 50 / top-p 0.95; DFlash/DFlash2 guide, Q3:
+ * temperature scaling of both logit sets before the acceptance ratio).  For
+ * each of the N rows: the K largest logits (the smaller id first on ties)
+ * with p_i = softmax(l / T) renormalised over those K; sorted by p (ties:
+ * smaller id first), the smallest prefix whose cumulative mass reaches
+ * top_p (at least one) is kept and renormalised, the rest of the K get 0.
+ *   logits [N, V] (dtype), 1 <= K <= V, T > 0;
+ *   ids [N, K] int32 ascending, probs [N, K] double;
+ *   flags [N] or NULL: ORACLE_FLAG_CDF_TIE when the cumulative mass at the
+ *   cut is within 1e-6 of top_p (either side), ORACLE_FLAG_INPUT_ERR (ids
+ *   -1, probs NaN) for a row with NaN, +inf or no finite logit.
+ */
+int oracle_support_topk(const void* logits, int dtype, int N, int V, double T, int K,
+                        double top_p, int32_t* ids, double* probs, uint32_t* flags,
+                        int nthreads);
+
 /* Threads the oracle would use for nthreads <= 0 (all online host cores). */
 int oracle_default_threads(void);
 
