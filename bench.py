@@ -215,7 +215,7 @@ def variant_lines(dev, stream):
     from rejection_sampling_gb300 import workloads as wl
     out = {}
     for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33",
-                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936"):
+                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936", "support_b64_g7_v128256"):
         d = wl.make(name, seed=0)
         copies = 8  # rotate over copies so the inputs exceed L2 where they are small
         calls = []
@@ -253,6 +253,17 @@ def variant_lines(dev, stream):
                 o = rs.CommitResult(torch.empty(B, W, dtype=torch.int32, device=dev),
                                     torch.empty(B, W, dtype=torch.int32, device=dev), None)
                 calls.append(rs.prepare_commit(*args, d["tau"], out=o, stream=stream))
+        elif d["kind"] == "support":
+            N, V, K = d["N"], d["V"], d["K"]
+            nbytes = N * V * (2 if d["dtype"] == "bf16" else 4)
+            positions = N
+            copies = 2  # 2 x 246 MB > L2
+            base = to_dev(d["logits"], dev)
+            for c in range(copies):
+                lg = base.clone()
+                o = rs.SupportResult(torch.empty(N, K, dtype=torch.int32, device=dev),
+                                     torch.empty(N, K, dtype=torch.float32, device=dev))
+                calls.append(rs.prepare_support(lg, d["T"], K, d["top_p"], out=o, stream=stream))
         elif d["kind"] == "sparse":
             B, G, k = d["B"], d["gamma"], d["kt"]
             nbytes = B * ((G + 1) * k + G * k) * 8 + B * G * 8 + B * 4
@@ -280,7 +291,7 @@ def variant_lines(dev, stream):
                      "positions_per_s": positions / (ms * 1e-3),
                      "GBps": nbytes / (ms * 1e-3) / 1e9,
                      "bytes_per_call": nbytes}
-        if d["kind"] in ("greedy", "commit"):  # streaming passes over logits: HBM roofline
+        if d["kind"] in ("greedy", "commit", "support"):  # streaming passes over logits: HBM roofline
             peak, _ = measured_peak()
             out[name]["frac_of_measured_hbm"] = out[name]["GBps"] / peak
         del calls

@@ -84,6 +84,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_VOCAB (1 << 24)
 #define SV_MAX_GAMMA 255  /* dense: gamma; any-order: W (and D <= SV_MAX_GAMMA * 64) */
 #define SV_MAX_LIST 4096  /* sparse: kt, kd */
+#define SV_MAX_TOPK 256   /* spec_support_topk: top_k */
 
 /* ABI version of this header; spec_verify_abi_version() returns it. */
 #define SV_ABI_VERSION 1
@@ -221,6 +222,26 @@ int spec_commit_confident(const void* logits, sv_dtype dtype, const int32_t* mas
                           int B, int W, int V, int32_t* commit, int32_t* tokens,
                           float* confidence, void* workspace, size_t ws_bytes,
                           sv_stream_t stream);
+
+/*
+ * spec_support_topk -- sparse support lists from dense logits: temperature,
+ * top-k, top-p (the Uno article's test setting, top-k 50 / top-p 0.95;
+ * DFlash/DFlash2 guide, Q3: both logit sets are temperature scaled before the
+ * acceptance ratio).  For each of the N rows of logits [N, V] (fp32 or bf16):
+ * the top_k largest logits (the smaller id first on ties) with probabilities
+ * softmax(l / temperature) renormalised over them; in decreasing probability
+ * the shortest prefix whose cumulative mass reaches top_p (at least one
+ * entry) is kept and renormalised, the rest get probability 0.
+ * Outputs: ids [N, top_k] int32 in ascending id order, probs [N, top_k] fp32
+ *   -- the lists spec_verify_sparse takes (target rows as tgt_ids/tgt_probs,
+ *   draft rows as drf_ids/drf_probs).  A row with NaN, +inf or no finite
+ *   logit gets ids -1 and probs NaN, and the status bit is set.
+ * Workspace: at least 256 bytes (the status word).  Limits: 1 <= top_k <=
+ * min(256, V); temperature > 0.
+ */
+int spec_support_topk(const void* logits, sv_dtype dtype, int N, int V, float temperature,
+                      int top_k, float top_p, int32_t* ids, float* probs, void* workspace,
+                      size_t ws_bytes, sv_stream_t stream);
 
 /*
  * spec_verify_check -- synchronise `stream`, read and clear the workspace

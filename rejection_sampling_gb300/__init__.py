@@ -11,6 +11,7 @@ hand-written CUDA kernels for sm_103a in libspec_verify.so:
   spec_verify_anyorder  masked-diffusion any-order window, small vocabulary
   spec_verify_greedy    greedy (temperature 0) verification: argmax match
   spec_commit_confident confidence-threshold commit of a block-diffusion pass
+  spec_support_topk     sparse support lists (temperature, top-k, top-p)
   spec_verify_dense_static  spec_verify_dense on a static scratch array, for
                         callers that cannot allocate device memory
 
@@ -20,11 +21,11 @@ call fails loudly if it is missing.  ``workloads`` generates the seeded
 synthetic inputs.
 """
 from ._binding import (  # noqa: F401
-    EXPORTED, CommitResult, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_SCRATCH_LIMIT,
+    EXPORTED, CommitResult, SupportResult, SV_BF16, SV_ERR_CUDA, SV_ERR_DEVICE_INPUT, SV_ERR_INVALID_ARG, SV_ERR_SCRATCH_LIMIT,
     SV_ERR_TIMEOUT, SV_ERR_UNSUPPORTED, SV_F32, SV_OK, SV_STATIC_SCRATCH_BYTES, SpecVerifyError,
     VerifyResult, abi_version, check,
     get_workspace, library_path, load, prepare_anyorder, prepare_commit, prepare_dense,
-    prepare_greedy, spec_commit_confident,
+    prepare_greedy, prepare_support, spec_commit_confident, spec_support_topk,
     prepare_sparse, PreparedCall, spec_verify_anyorder, spec_verify_dense,
     spec_verify_dense_static, spec_verify_greedy, spec_verify_sparse, status_string,
     workspace_size,

@@ -27,7 +27,7 @@ EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
     "spec_verify_status_string", "spec_verify_dense_static", "spec_verify_greedy",
-    "spec_commit_confident",
+    "spec_commit_confident", "spec_support_topk",
 )
 
 
@@ -79,6 +79,8 @@ def load(build_if_missing: bool = False):
         lib.spec_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, Z, P]
         lib.spec_commit_confident.restype = I
         lib.spec_commit_confident.argtypes = [P, I, P, ctypes.c_float, I, I, I, P, P, P, P, Z, P]
+        lib.spec_support_topk.restype = I
+        lib.spec_support_topk.argtypes = [P, I, I, I, ctypes.c_float, I, ctypes.c_float, P, P, P, Z, P]
         lib.spec_verify_dense_static.restype = I
         lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         _lib = lib
@@ -280,6 +282,59 @@ def prepare_commit(logits, masked, tau: float, out: CommitResult,
             _ptr(out.commit), _ptr(out.tokens), _ptr(out.confidence), ws.data_ptr(), ws.numel(), sp)
     keep = (logits, masked, out, ws)
     return PreparedCall(lib.spec_commit_confident, args, keep, "spec_commit_confident")
+
+
+class SupportResult(NamedTuple):
+    ids: torch.Tensor
+    probs: torch.Tensor
+
+
+def spec_support_topk(logits: torch.Tensor, temperature: float, top_k: int, top_p: float, *,
+                      out: Optional[SupportResult] = None,
+                      stream: Optional[torch.cuda.Stream] = None) -> SupportResult:
+    """Sparse support lists from dense logits [..., V] (bf16 or fp32, CUDA):
+    ids [..., top_k] ascending, probs [..., top_k]."""
+    lib = load()
+    dev = logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_support_topk needs CUDA tensors")
+    dt = _logit_dtype(logits)
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    lead = tuple(logits.shape[:-1])
+    V = int(logits.shape[-1])
+    N = 1
+    for d in lead:
+        N *= int(d)
+    K = int(top_k)
+    if out is None:
+        out = SupportResult(torch.empty(lead + (K,), dtype=torch.int32, device=dev),
+                            torch.empty(lead + (K,), dtype=torch.float32, device=dev))
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_support_topk(_ptr(logits), dt, N, V, float(temperature), K, float(top_p),
+                                   _ptr(out.ids), _ptr(out.probs), ws.data_ptr(), ws.numel(), sp)
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_support_topk")
+    return out
+
+
+def prepare_support(logits, temperature: float, top_k: int, top_p: float, out: SupportResult,
+                    stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """Validate once and return a PreparedCall repeating spec_support_topk."""
+    spec_support_topk(logits, temperature, top_k, top_p, out=out, stream=stream)
+    lib = load()
+    dev = logits.device
+    V = int(logits.shape[-1])
+    N = logits.numel() // V
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    args = (_ptr(logits), _logit_dtype(logits), N, V, ctypes.c_float(float(temperature)),
+            int(top_k), ctypes.c_float(float(top_p)), _ptr(out.ids), _ptr(out.probs),
+            ws.data_ptr(), ws.numel(), sp)
+    keep = (logits, out, ws)
+    return PreparedCall(lib.spec_support_topk, args, keep, "spec_support_topk")
 
 
 def prepare_greedy(target_logits, draft_ids, out: VerifyResult,

@@ -2,6 +2,7 @@
 // argument validation, kernel selection, workspace layout, status word.
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <math.h>
 #include <string.h>
 
 #include "../../include/spec_verify.h"
@@ -189,6 +190,26 @@ int spec_commit_confident(const void* logits, sv_dtype dtype, const int32_t* mas
   p.bf16 = (dtype == SV_BF16);
   p.aligned = ((size_t)V * es) % 16 == 0 && aligned_to(logits, 16);
   return launch_status(sv::launch_commit(p, tau, commit, confidence, (cudaStream_t)stream));
+}
+
+int spec_support_topk(const void* logits, sv_dtype dtype, int N, int V, float temperature,
+                      int top_k, float top_p, int32_t* ids, float* probs, void* workspace,
+                      size_t ws_bytes, sv_stream_t stream) {
+  if (N < 0 || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if (top_k < 1 || top_k > SV_MAX_TOPK || top_k > V) return SV_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(temperature < INFINITY) || top_p != top_p) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (N == 0) return SV_OK;
+  if (!logits || !ids || !probs || !workspace || ws_bytes < sizeof(sv::WsHeader)) return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(logits, es) || !aligned_to(ids, 4) || !aligned_to(probs, 4) ||
+      !aligned_to(workspace, 256))
+    return SV_ERR_INVALID_ARG;
+  sv::WsHeader* hdr = reinterpret_cast<sv::WsHeader*>(workspace);
+  const int aligned = ((size_t)V * es) % 16 == 0 && aligned_to(logits, 16);
+  return launch_status(sv::launch_support(static_cast<const unsigned char*>(logits), N, V, top_k,
+                                          dtype == SV_BF16, aligned, temperature, top_p, ids,
+                                          probs, &hdr->status, (cudaStream_t)stream));
 }
 
 int spec_verify_sparse(const int32_t* tgt_ids, const float* tgt_probs, int kt,

@@ -158,6 +158,10 @@ cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s);  // greedy: tar
 // p.G = W - 1, p.tok_out = tokens [B, W]
 cudaError_t launch_commit(const DenseParams& p, float tau, int32_t* commit, float* confidence,
                           cudaStream_t s);
+// sparse support lists (temperature, top-k, top-p) from dense logits [N, V]
+cudaError_t launch_support(const unsigned char* lt, int N, int V, int K, int bf16, int aligned,
+                           float temperature, float top_p, int32_t* ids, float* probs,
+                           uint32_t* status, cudaStream_t s);
 cudaError_t launch_small(const SmallParams& p, cudaStream_t s);
 size_t small_smem_per_warp(int R, int vstride);
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s);

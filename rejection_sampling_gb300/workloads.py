@@ -32,6 +32,9 @@ Workloads (sizes and distributions of the five verification workloads):
 ``greedy_b64_g7_v128256``  greedy (T = 0) verification on the headline shape:
                            B=64, gamma=7, V=128256, bf16 target ~ N(0, 3^2);
                            draft ids = argmax of target + N(0, 0.5^2).
+``support_b64_g7_v128256`` sparse support lists (temperature 1, top-k 50,
+                           top-p 0.95) for the 64 x (8 + 7) target and draft
+                           rows of ``dense_b64_g7_v128256``.
 ``commit_b64_w4_v151936``  confidence-threshold commit: 64 blocks of 4
                            positions (SDAR block length), V=151936, bf16
                            logits ~ N(0, 3^2) plus one spike of height
@@ -310,6 +313,7 @@ WORKLOADS = {
     "greedy_b64_g7_v128256": dict(kind="greedy", B=64, gamma=7, V=128256, dtype="bf16",
                                   target_sigma=3.0, draft_noise=0.5),
     "commit_b64_w4_v151936": dict(kind="commit", B=64, W=4, V=151936, dtype="bf16"),
+    "support_b64_g7_v128256": dict(kind="support", B=64, gamma=7, V=128256, dtype="bf16"),
 }
 
 
@@ -330,6 +334,14 @@ def make(name: str, seed: int = 0, **override) -> dict:
     elif kind == "commit":
         B, W, V = cfg.pop("B"), cfg.pop("W"), cfg.pop("V")
         d = commit_inputs(B, W, V, seed=seed, **cfg)
+    elif kind == "support":
+        # the headline's target and draft rows, preprocessed with the Uno
+        # article's test setting (temperature 1, top-k 50, top-p 0.95)
+        B, g, V = cfg.pop("B"), cfg.pop("gamma"), cfg.pop("V")
+        dd = dense_inputs(B, g, V, seed=seed, dtype=cfg.pop("dtype"))
+        rows = np.concatenate([dd["target"].reshape(-1, V), dd["draft"].reshape(-1, V)])
+        d = dict(kind="support", dtype=dd["dtype"], N=rows.shape[0], V=V, K=50, T=1.0,
+                 top_p=0.95, logits=np.ascontiguousarray(rows))
     else:
         B, D, W, V = cfg.pop("B"), cfg.pop("D"), cfg.pop("W"), cfg.pop("V")
         d = anyorder_inputs(B, D, W, V, seed=seed, **cfg)
