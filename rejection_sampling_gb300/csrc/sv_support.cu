@@ -19,8 +19,8 @@
 // and only compare each 16-byte vector's largest element with a threshold --
 // a value that at least K elements of the row reach, so it never exceeds the
 // K-th largest logit.  It starts as the K-th largest of the CTA's 256 lane
-// maxima over the first chunk round.  A vector that reaches it is parked (its
-// index only); parked vectors are expanded into 64-bit keys -- the logit's
+// maxima over the first two chunk rounds.  A vector that reaches it is parked
+// (its index only); parked vectors are expanded into 64-bit keys -- the logit's
 // order-preserving bits above the complemented id, so one unsigned comparison
 // orders by value, then by the smaller id -- only when the parking buffer
 // fills (then a warp's keys may be cut back to its top K, raising its
@@ -510,17 +510,20 @@ __global__ void __launch_bounds__(32 * W, 3)
   }
 
   // The starting threshold: the K-th largest of the CTA's 32 W lane maxima
-  // over its first chunk round.  Those maxima are distinct elements of the
-  // row, so at least K elements reach it: it never exceeds the row's K-th
-  // largest logit.
+  // over its first kRStages chunk rounds (the filled stages).  Those maxima
+  // are distinct elements of the row, so at least K elements reach it: it
+  // never exceeds the row's K-th largest logit.
   uint32_t w[kU][4];
-  if (P.aligned) cp_async_wait_group<kRStages - 1>();
-  read_chunk(ring, base, warp, nfull, nvec, V, P.bf16, P.aligned, lane, w);  // -inf past the row
   float thr;
   {
+    if (P.aligned) cp_async_wait_group<0>();
     float tm = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < kU; ++u) tm = fmaxf(tm, vec_max(w[u], P.bf16));  // NaN ignored here
+    for (int st = kRStages - 1; st >= 0; --st) {  // ends with chunk `warp` (stage 0) in w
+      read_chunk(ring + st * kChunkB, base, warp + st * W, nfull, nvec, V, P.bf16, P.aligned, lane, w);
+#pragma unroll
+      for (int u = 0; u < kU; ++u) tm = fmaxf(tm, vec_max(w[u], P.bf16));  // NaN ignored here
+    }
     cta_kth_of_lanes<W>(tm, K, s_lv, &s_thr, warp, lane);
     thr = s_thr;
   }
