@@ -526,8 +526,8 @@ def run_reference(args):
 
 def run_calls_only(args):
     """Profiling driver: args.calls_only untimed calls of one workload (the
-    headline by default; ``--workload greedy_b64_g7_v128256`` for the greedy
-    path), no output beyond one status line (ncu's launch filters pick the
+    headline by default; ``--workload NAME`` for the greedy, commit and
+    support paths), no output beyond one status line (ncu's launch filters pick the
     kernels out)."""
     import torch
     import rejection_sampling_gb300 as rs
@@ -546,8 +546,11 @@ def run_calls_only(args):
     elif d["kind"] == "commit":
         t = [to_dev(d[k], dev) for k in ("logits", "masked")] + [d["tau"]]
         fn = rs.spec_commit_confident
+    elif d["kind"] == "support":
+        t = [to_dev(d["logits"], dev), d["T"], d["K"], d["top_p"]]
+        fn = rs.spec_support_topk
     else:
-        raise SystemExit(f"--calls-only drives dense, greedy and commit workloads, not {name}")
+        raise SystemExit(f"--calls-only drives dense, greedy, commit and support workloads, not {name}")
     for _ in range(args.calls_only):
         fn(*t)
     torch.cuda.synchronize()
