@@ -63,9 +63,11 @@ def _load():
             lib.oracle_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, I]
             lib.oracle_commit_confident.argtypes = [P, I, P, ctypes.c_double, I, I, I, P, P, P, P, I]
             lib.oracle_support_topk.argtypes = [P, I, I, I, ctypes.c_double, I, ctypes.c_double, P, P, P, I]
+            lib.oracle_anyorder_rounds.argtypes = [P, P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, I]
+            lib.oracle_cosine_window.argtypes = [I, I, ctypes.c_double]
             for f in (lib.oracle_verify_dense, lib.oracle_verify_sparse, lib.oracle_verify_anyorder,
                       lib.oracle_verify_greedy, lib.oracle_commit_confident,
-                      lib.oracle_support_topk):
+                      lib.oracle_support_topk, lib.oracle_anyorder_rounds, lib.oracle_cosine_window):
                 f.restype = I
             lib.oracle_default_threads.restype = I
             _lib = lib
@@ -236,3 +238,39 @@ def verify_anyorder(target, draft, order, draft_tokens, u_accept, u_sample, *, o
     if rc != 0:
         raise RuntimeError("oracle_verify_anyorder failed")
     return out
+
+
+def anyorder_rounds(target, draft, order, revealed, window, draft_tokens, u_accept, u_sample, *,
+                    tokens_init=None, nthreads: int = 0) -> dict:
+    """Windowed multi-round any-order verification.  target [B, R, D, V],
+    draft [B, D, V], order [B, D], revealed [B], window [B], draft_tokens
+    [B, R, D], u_accept [B, R, D] (by sigma index), u_sample [B, R]."""
+    lib = _load()
+    lt, dt = _logits(target)
+    ld, dt2 = _logits(draft)
+    assert dt == dt2
+    B, R, D, V = lt.shape
+    assert ld.shape == (B, D, V)
+    sig = np.ascontiguousarray(order, dtype=np.int32).reshape(B, D)
+    i0 = np.ascontiguousarray(revealed, dtype=np.int32).reshape(B)
+    win = np.ascontiguousarray(window, dtype=np.int32).reshape(B)
+    tok = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, R, D)
+    ua = np.ascontiguousarray(u_accept, dtype=np.float32).reshape(B, R, D)
+    us = np.ascontiguousarray(u_sample, dtype=np.float32).reshape(B, R)
+    out = dict(tokens=(np.full((B, D), -7, np.int32) if tokens_init is None
+                       else np.array(tokens_init, dtype=np.int32, copy=True)),
+               n_revealed=np.zeros(B, np.int32),
+               round_accepts=np.zeros((B, R), np.int32),
+               flags=np.zeros(B, np.uint32))
+    rc = lib.oracle_anyorder_rounds(_ptr(lt), _ptr(ld), dt, _ptr(sig), _ptr(i0), _ptr(win),
+                                    _ptr(tok), _ptr(ua), _ptr(us), B, R, D, V,
+                                    _ptr(out["tokens"]), _ptr(out["n_revealed"]),
+                                    _ptr(out["round_accepts"]), _ptr(out["flags"]), int(nthreads))
+    if rc != 0:
+        raise RuntimeError("oracle_anyorder_rounds failed")
+    return out
+
+
+def cosine_window(D: int, i: int, dtau: float) -> int:
+    """W(i): the window of an outer step starting with i of D tokens revealed."""
+    return int(_load().oracle_cosine_window(int(D), int(i), float(dtau)))

@@ -830,3 +830,148 @@ int oracle_support_topk(const void* logits, int dtype, int N, int V, double T, i
   support_args a = {logits, dtype, N, V, K, T, top_p, ids, probs, flags};
   return run_rows(support_row, &a, N, 2 * (size_t)V, nthreads);
 }
+
+/* ------------------------------------------------------------------ */
+/* Windowed multi-round any-order verification                          */
+/* ------------------------------------------------------------------ */
+/* [SSMD4] ("Self-Speculative Masked Diffusions", key design 4, windowed
+ * multi-round verification).  One non-causal pass gives the draft
+ * distributions of the window W(i); several causal verification rounds then
+ * run on them.  Each round verifies the still-masked window positions in
+ * sigma order against that round's target distributions with that round's
+ * draft tokens (after a resample the later drafts change, and the causal
+ * probabilities are recomputed); it ends at its first rejection, whose
+ * position is resampled from max(p - q, 0) renormalised and revealed (the
+ * any-order rule, key design 2); the next round starts after it.  A round
+ * that accepts every remaining draft closes the window.  No bonus token.
+ *
+ * Input errors are raised where the rounds use an input: an out-of-range or
+ * repeated sigma entry inside the window (checked first), a revealed count
+ * outside [0, D], a window below 1, and -- as the rounds reach them -- a
+ * draft token out of range or a logit row with NaN, +inf or no finite
+ * entry. */
+typedef struct {
+  const void *lt, *ld;
+  int dtype;
+  const int32_t *order, *i0, *win, *tok_in;
+  const float *u_acc, *u_s;
+  int B, R, D, V;
+  int32_t *tok_out, *n_out, *racc_out;
+  uint32_t* flags;
+} rounds_args;
+
+static void rounds_row(const void* pa, int b, double* scratch) {
+  const rounds_args* a = (const rounds_args*)pa;
+  const int R = a->R, D = a->D, V = a->V;
+  double* p = scratch;
+  double* q = p + V;
+  double* w = q + V;
+  uint32_t flag = 0;
+  const int32_t* sig = a->order + (size_t)b * D;
+  int32_t* out = a->tok_out + (size_t)b * D;
+  int32_t* racc = a->racc_out + (size_t)b * R;
+  const int i0 = a->i0[b], W = a->win[b];
+  for (int r = 0; r < R; ++r) racc[r] = -1;
+
+  int bad = (i0 < 0 || i0 > D || W < 1);
+  const int e = bad ? 0 : ((W > D - i0) ? D : i0 + W); /* the window is sigma[i0, e) */
+  for (int k = i0; k < e && !bad; ++k) {
+    if (sig[k] < 0 || sig[k] >= D) bad = 1;
+    for (int k2 = i0; k2 < k && !bad; ++k2)
+      if (sig[k2] == sig[k]) bad = 1;
+  }
+
+  int i = i0; /* sigma index of the first still-masked window position */
+  for (int r = 0; r < R && !bad && i < e; ++r) {
+    const size_t rr = ((size_t)b * R + r) * (size_t)D; /* round r's [D] slice */
+    const size_t dd = (size_t)b * (size_t)D;
+    int stop = e;
+    for (int k = i; k < e; ++k) {
+      const int32_t s = sig[k];
+      const int32_t x = a->tok_in[rr + s];
+      if (x < 0 || x >= V || check_row(a->lt, a->dtype, (rr + s) * (size_t)V, V) ||
+          check_row(a->ld, a->dtype, (dd + s) * (size_t)V, V)) {
+        bad = 1;
+        break;
+      }
+      softmax_row(a->lt, a->dtype, (rr + s) * (size_t)V, V, p);
+      softmax_row(a->ld, a->dtype, (dd + s) * (size_t)V, V, q);
+      if (!accept_test(p[x], q[x], a->u_acc[rr + k], NULL, &flag)) {
+        stop = k; /* p and q now hold this position's distributions */
+        break;
+      }
+    }
+    if (bad) break;
+    for (int k = i; k < stop; ++k) out[sig[k]] = a->tok_in[rr + sig[k]];
+    racc[r] = stop - i;
+    if (stop < e) {
+      for (int v = 0; v < V; ++v) {
+        const double d = p[v] - q[v];
+        w[v] = d > 0.0 ? d : 0.0;
+      }
+      const float us = a->u_s[(size_t)b * R + r];
+      int y = inverse_cdf(w, V, us, NULL, &flag);
+      if (y < 0) {
+        flag |= ORACLE_FLAG_ZERO_RESID;
+        y = inverse_cdf(p, V, us, NULL, &flag);
+      }
+      out[sig[stop]] = y;
+      i = stop + 1;
+    } else {
+      i = e;
+    }
+  }
+
+  if (bad) {
+    for (int k = (i0 >= 0 ? i0 : 0); k < e; ++k)
+      if (sig[k] >= 0 && sig[k] < D) out[sig[k]] = -1;
+    for (int r = 0; r < R; ++r) racc[r] = -1;
+    a->n_out[b] = -1;
+    if (a->flags) a->flags[b] = ORACLE_FLAG_INPUT_ERR;
+    return;
+  }
+  a->n_out[b] = i;
+  if (a->flags) a->flags[b] = flag;
+}
+
+int oracle_anyorder_rounds(const void* target_logits, const void* draft_logits, int dtype,
+                           const int32_t* order, const int32_t* revealed, const int32_t* window,
+                           const int32_t* draft_tokens, const float* u_accept,
+                           const float* u_sample, int B, int R, int D, int V, int32_t* tokens,
+                           int32_t* n_revealed, int32_t* round_accepts, uint32_t* flags,
+                           int nthreads) {
+  if (B < 0 || R <= 0 || D <= 0 || V <= 0) return -1;
+  if (B == 0) return 0;
+  if (!target_logits || !draft_logits || !order || !revealed || !window || !draft_tokens ||
+      !u_accept || !u_sample || !tokens || !n_revealed || !round_accepts)
+    return -1;
+  if (dtype != ORACLE_F32 && dtype != ORACLE_BF16) return -1;
+  rounds_args a = {target_logits, draft_logits, dtype,    order,      revealed,
+                   window,        draft_tokens, u_accept, u_sample,   B,
+                   R,             D,            V,        tokens,     n_revealed,
+                   round_accepts, flags};
+  return run_rows(rounds_row, &a, B, 3 * (size_t)V, nthreads);
+}
+
+/* [SSMD4] The window W(i) of the outer step that starts with i of D tokens
+ * revealed: the page has it grow with i, cosine-shaped, set by dtau.  Reading:
+ * the positions a cosine-schedule masked-diffusion sampler reveals over the
+ * next dtau of its time.  Its revealed fraction at time t in [0, 1] is
+ * f(t) = 1 - cos(pi t / 2) (slow at first, faster later); t(i) solves
+ * f(t) = i / D; W(i) = ceil(D f(min(1, t(i) + dtau)) - 1e-9) - i, at least 1,
+ * at most D - i (the 1e-9 keeps a product that rounds just above an integer
+ * from adding a position).  0 when i >= D. */
+int oracle_cosine_window(int D, int i, double dtau) {
+  if (D <= 0 || i < 0) return -1;
+  if (i >= D) return 0;
+  const double pi = 3.14159265358979323846;
+  const double t = (2.0 / pi) * acos(1.0 - (double)i / (double)D);
+  double t1 = t + (dtau > 0.0 ? dtau : 0.0);
+  if (t1 > 1.0) t1 = 1.0;
+  const double reach = (double)D * (1.0 - cos(0.5 * pi * t1));
+  long long end = (long long)ceil(reach - 1e-9);
+  if (end > D) end = D;
+  long long wv = end - i;
+  if (wv < 1) wv = 1;
+  return (int)wv;
+}

@@ -151,6 +151,40 @@ int oracle_support_topk(const void* logits, int dtype, int N, int V, double T, i
                         double top_p, int32_t* ids, double* probs, uint32_t* flags,
                         int nthreads);
 
+/* Windowed multi-round any-order verification ("Self-Speculative Masked
+ * Diffusions", key design 4): one non-causal pass drafts the window, several
+ * causal verification rounds run on it.  Round r verifies the still-masked
+ * window positions in sigma order against round r's target logits with
+ * round r's draft tokens, ends at its first rejection with a resample from
+ * max(p - q, 0) (revealed too), and the next round starts after it; a round
+ * that accepts every remaining draft closes the window.  No bonus token.
+ *   target_logits [B, R, D, V]  round r's target logits per sequence position
+ *   draft_logits  [B, D, V]     the window's draft logits (every round)
+ *   order [B, D]  sigma; revealed [B] = i0 (sigma[0, i0) already revealed);
+ *   window [B] >= 1: the window is sigma[i0, min(D, i0 + window))
+ *   draft_tokens [B, R, D]      round r's draft token per sequence position
+ *   u_accept [B, R, D]          round r's accept uniform, by sigma index
+ *   u_sample [B, R]             round r's residual uniform
+ * Outputs: tokens [B, D] (each revealed token at its position; others left
+ * as they are; the window's positions -1 on an input error); n_revealed [B]
+ * (i0 + the tokens the rounds revealed, -1 on an input error);
+ * round_accepts [B, R] (drafts accepted in round r, -1 for rounds not run);
+ * flags [B] or NULL (accept band, CDF tie, zero residual, input error).
+ */
+int oracle_anyorder_rounds(const void* target_logits, const void* draft_logits, int dtype,
+                           const int32_t* order, const int32_t* revealed, const int32_t* window,
+                           const int32_t* draft_tokens, const float* u_accept,
+                           const float* u_sample, int B, int R, int D, int V, int32_t* tokens,
+                           int32_t* n_revealed, int32_t* round_accepts, uint32_t* flags,
+                           int nthreads);
+
+/* The window W(i) of an outer step starting with i of D tokens revealed
+ * (same page, key design 4: it grows with i, cosine-shaped, set by dtau):
+ * the positions a cosine-schedule masked-diffusion sampler (revealed
+ * fraction 1 - cos(pi t / 2) at time t) reveals over the next dtau of its
+ * time, at least 1 and at most D - i; 0 when i >= D, -1 on bad arguments. */
+int oracle_cosine_window(int D, int i, double dtau);
+
 /* Threads the oracle would use for nthreads <= 0 (all online host cores). */
 int oracle_default_threads(void);
 
