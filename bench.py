@@ -215,7 +215,8 @@ def variant_lines(dev, stream):
     from rejection_sampling_gb300 import workloads as wl
     out = {}
     for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33",
-                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936", "support_b64_g7_v128256"):
+                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936", "support_b64_g7_v128256",
+                 "rounds_b4096_r4_d256_v27"):
         d = wl.make(name, seed=0)
         copies = 8  # rotate over copies so the inputs exceed L2 where they are small
         calls = []
@@ -264,6 +265,24 @@ def variant_lines(dev, stream):
                 o = rs.SupportResult(torch.empty(N, K, dtype=torch.int32, device=dev),
                                      torch.empty(N, K, dtype=torch.float32, device=dev))
                 calls.append(rs.prepare_support(lg, d["T"], K, d["top_p"], out=o, stream=stream))
+        elif d["kind"] == "rounds":
+            B, R, D, V = d["B"], d["R"], d["D"], d["V"]
+            window = np.array([rs.spec_anyorder_window(D, int(i), d["dtau"]) for i in d["revealed"]],
+                              np.int32)
+            base = [to_dev(x, dev) for x in (d["target"], d["draft"], d["order"], d["revealed"], window,
+                                             d["draft_tokens"], d["u_accept"], d["u_sample"])]
+            copies = 2  # the rows a call reads are scattered; two copies alternate anyway
+            for c in range(copies):
+                args = [t.clone() for t in base]
+                o = rs.RoundsResult(torch.full((B, D), -1, dtype=torch.int32, device=dev),
+                                    torch.empty(B, dtype=torch.int32, device=dev),
+                                    torch.empty(B, R, dtype=torch.int32, device=dev))
+                calls.append(rs.prepare_rounds(*args, out=o, stream=stream))
+            torch.cuda.synchronize()
+            revealed = int((o.n_revealed - base[3]).sum())
+            # every revealed position's target row (its round) and draft row is read once
+            nbytes = 2 * revealed * V * (2 if d["dtype"] == "bf16" else 4)
+            positions = revealed
         elif d["kind"] == "sparse":
             B, G, k = d["B"], d["gamma"], d["kt"]
             nbytes = B * ((G + 1) * k + G * k) * 8 + B * G * 8 + B * 4

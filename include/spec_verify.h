@@ -181,6 +181,57 @@ int spec_verify_anyorder(const void* target_logits, const void* draft_logits, sv
                          sv_stream_t stream);
 
 /*
+ * spec_verify_anyorder_rounds -- windowed multi-round any-order verification
+ * (Self-Speculative Masked Diffusions, key design 4: one non-causal pass
+ * drafts the window, several causal verification rounds run on it).  For
+ * sequence b the window is sigma[i0, e), i0 = revealed[b],
+ * e = min(D, i0 + window[b]).  Round r (r = 0 .. R-1) starts at sigma index
+ * i_r (i_0 = i0): it verifies positions s = sigma[k], k = i_r, i_r + 1, ...
+ * in order with p = softmax(target_logits[b, r, s]),
+ * q = softmax(draft_logits[b, s]), x = draft_tokens[b, r, s] and
+ * u = u_accept[b, r, k] (accept iff u < min(1, p(x)/q(x)), ratio 0 when
+ * q(x) = 0); at the first rejection it draws the replacement from
+ * max(p - q, 0) renormalised by inverse CDF over ascending ids with
+ * u_sample[b, r] and i_{r+1} = that index + 1; a round that accepts every
+ * remaining draft closes the window.  No bonus token.
+ *   target_logits [B, R, D, V] and draft_logits [B, D, V], fp32 or bf16, in
+ *     sequence-position order (only the rows the rounds reach are read);
+ *   order [B, D] sigma; revealed [B]; window [B] (>= 1; see
+ *     spec_anyorder_window); draft_tokens [B, R, D]; u_accept [B, R, D]
+ *     (indexed by sigma index); u_sample [B, R]; uniforms in [0, 1).
+ * Outputs: tokens [B, D]: each revealed token at its position, other
+ *   entries untouched; n_revealed [B] = i0 + the tokens the rounds revealed;
+ *   round_accepts [B, R]: drafts accepted by round r, -1 for rounds not run.
+ *   An input error (revealed outside [0, D], window < 1, a sigma entry in the
+ *   window out of range or repeated, or -- where a round reaches it -- a
+ *   draft token out of range or a logit row with NaN, +inf or no finite
+ *   entry) gives n_revealed -1, round_accepts -1 and -1 at the window's
+ *   positions, and sets the status bit.
+ * Workspace: the status word only (any workspace of at least 256 bytes).
+ * Host errors: B, D, V < 0 or 0 (B = 0 is a no-op), R < 1, D * V or
+ * B * R * D beyond 2^31, dtype, null or misaligned pointers.
+ */
+int spec_verify_anyorder_rounds(const void* target_logits, const void* draft_logits,
+                                sv_dtype dtype, const int32_t* order, const int32_t* revealed,
+                                const int32_t* window, const int32_t* draft_tokens,
+                                const float* u_accept, const float* u_sample, int B, int R, int D,
+                                int V, int32_t* tokens, int32_t* n_revealed,
+                                int32_t* round_accepts, void* workspace, size_t ws_bytes,
+                                sv_stream_t stream);
+
+/*
+ * spec_anyorder_window -- the window W(i) of an outer step that starts with
+ * i of D tokens revealed (same page, key design 4: it grows with i,
+ * cosine-shaped, set by dtau).  Reading taken: the positions a
+ * cosine-schedule masked-diffusion sampler, revealed fraction
+ * f(t) = 1 - cos(pi t / 2) at time t in [0, 1], reveals over the next dtau
+ * of its time: W = ceil(D f(min(1, t(i) + dtau)) - 1e-9) - i with
+ * f(t(i)) = i / D, at least 1 and at most D - i.  Host function (no device
+ * work); returns 0 when i >= D and -1 for D < 1 or i < 0.
+ */
+int spec_anyorder_window(int D, int revealed, float dtau);
+
+/*
  * spec_verify_greedy -- greedy (temperature 0) verification (DFlash/DFlash2
  * guide, 4.4: under greedy decoding a draft token is accepted if and only if
  * it is the target's choice; the page's formula is lost, and this is the

@@ -12,6 +12,9 @@ hand-written CUDA kernels for sm_103a in libspec_verify.so:
   spec_verify_greedy    greedy (temperature 0) verification: argmax match
   spec_commit_confident confidence-threshold commit of a block-diffusion pass
   spec_support_topk     sparse support lists (temperature, top-k, top-p)
+  spec_verify_anyorder_rounds  windowed multi-round any-order verification
+                        (several rounds on one window of draft distributions)
+  spec_anyorder_window  the cosine-schedule window W(i) (host function)
   spec_verify_dense_static  spec_verify_dense on a static scratch array, for
                         callers that cannot allocate device memory
 
@@ -26,6 +29,7 @@ from ._binding import (  # noqa: F401
     VerifyResult, abi_version, check,
     get_workspace, library_path, load, prepare_anyorder, prepare_commit, prepare_dense,
     prepare_greedy, prepare_support, spec_commit_confident, spec_support_topk,
+    RoundsResult, prepare_rounds, spec_anyorder_window, spec_verify_anyorder_rounds,
     prepare_sparse, PreparedCall, spec_verify_anyorder, spec_verify_dense,
     spec_verify_dense_static, spec_verify_greedy, spec_verify_sparse, status_string,
     workspace_size,

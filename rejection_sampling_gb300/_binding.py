@@ -27,7 +27,8 @@ EXPORTED = (
     "spec_verify_abi_version", "spec_verify_workspace_size", "spec_verify_workspace_init",
     "spec_verify_dense", "spec_verify_sparse", "spec_verify_anyorder", "spec_verify_check",
     "spec_verify_status_string", "spec_verify_dense_static", "spec_verify_greedy",
-    "spec_commit_confident", "spec_support_topk",
+    "spec_commit_confident", "spec_support_topk", "spec_verify_anyorder_rounds",
+    "spec_anyorder_window",
 )
 
 
@@ -81,6 +82,10 @@ def load(build_if_missing: bool = False):
         lib.spec_commit_confident.argtypes = [P, I, P, ctypes.c_float, I, I, I, P, P, P, P, Z, P]
         lib.spec_support_topk.restype = I
         lib.spec_support_topk.argtypes = [P, I, I, I, ctypes.c_float, I, ctypes.c_float, P, P, P, Z, P]
+        lib.spec_verify_anyorder_rounds.restype = I
+        lib.spec_verify_anyorder_rounds.argtypes = [P, P, I, P, P, P, P, P, P, I, I, I, I, P, P, P, P, Z, P]
+        lib.spec_anyorder_window.restype = I
+        lib.spec_anyorder_window.argtypes = [I, I, ctypes.c_float]
         lib.spec_verify_dense_static.restype = I
         lib.spec_verify_dense_static.argtypes = [P, P, I, P, P, P, I, I, I, P, P, P, P, P]
         _lib = lib
@@ -472,6 +477,72 @@ def spec_verify_anyorder(target_logits: torch.Tensor, draft_logits: torch.Tensor
     return res
 
 
+class RoundsResult(NamedTuple):
+    tokens: torch.Tensor         # [B, D] int32, revealed tokens written at their positions
+    n_revealed: torch.Tensor     # [B] int32
+    round_accepts: torch.Tensor  # [B, R] int32
+
+
+def _rounds_args(target_logits, draft_logits, order, revealed, window, draft_tokens, u_accept,
+                 u_sample, out: RoundsResult, ws, sp):
+    B, R, D, V = (int(v) for v in target_logits.shape)
+    return (_ptr(target_logits), _ptr(draft_logits), _logit_dtype(target_logits), _ptr(order),
+            _ptr(revealed), _ptr(window), _ptr(draft_tokens), _ptr(u_accept), _ptr(u_sample),
+            B, R, D, V, _ptr(out.tokens), _ptr(out.n_revealed), _ptr(out.round_accepts),
+            ws.data_ptr(), ws.numel(), sp)
+
+
+def spec_verify_anyorder_rounds(target_logits: torch.Tensor, draft_logits: torch.Tensor,
+                                order: torch.Tensor, revealed: torch.Tensor, window: torch.Tensor,
+                                draft_tokens: torch.Tensor, u_accept: torch.Tensor,
+                                u_sample: torch.Tensor, *, tokens: Optional[torch.Tensor] = None,
+                                out: Optional[RoundsResult] = None,
+                                stream: Optional[torch.cuda.Stream] = None) -> RoundsResult:
+    """Windowed multi-round any-order verification.  target [B, R, D, V],
+    draft [B, D, V], order [B, D], revealed [B], window [B], draft_tokens
+    [B, R, D], u_accept [B, R, D] (by sigma index), u_sample [B, R].  tokens
+    [B, D] is updated in place at the revealed positions (allocated filled
+    with -1 if not given)."""
+    lib = load()
+    dev = target_logits.device
+    if dev.type != "cuda":
+        raise ValueError("spec_verify_anyorder_rounds needs CUDA tensors")
+    B, R, D, V = target_logits.shape
+    _req(target_logits, "target_logits", target_logits.dtype, (B, R, D, V), dev)
+    _logit_dtype(target_logits)
+    _req(draft_logits, "draft_logits", target_logits.dtype, (B, D, V), dev)
+    _req(order, "order", torch.int32, (B, D), dev)
+    _req(revealed, "revealed", torch.int32, (B,), dev)
+    _req(window, "window", torch.int32, (B,), dev)
+    _req(draft_tokens, "draft_tokens", torch.int32, (B, R, D), dev)
+    _req(u_accept, "u_accept", torch.float32, (B, R, D), dev)
+    _req(u_sample, "u_sample", torch.float32, (B, R), dev)
+    if out is None:
+        if tokens is None:
+            tokens = torch.full((B, D), -1, dtype=torch.int32, device=dev)
+        out = RoundsResult(tokens, torch.empty(B, dtype=torch.int32, device=dev),
+                           torch.empty(B, R, dtype=torch.int32, device=dev))
+    _req(out.tokens, "tokens", torch.int32, (B, D), dev)
+    _req(out.n_revealed, "n_revealed", torch.int32, (B,), dev)
+    _req(out.round_accepts, "round_accepts", torch.int32, (B, R), dev)
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    with torch.cuda.device(dev):
+        rc = lib.spec_verify_anyorder_rounds(*_rounds_args(target_logits, draft_logits, order, revealed,
+                                                           window, draft_tokens, u_accept, u_sample,
+                                                           out, ws, sp))
+    if rc != SV_OK:
+        raise SpecVerifyError(rc, "spec_verify_anyorder_rounds")
+    return out
+
+
+def spec_anyorder_window(D: int, revealed: int, dtau: float) -> int:
+    """W(i): the window of an outer step starting with `revealed` of D tokens
+    revealed (cosine schedule, step dtau); computed by the library's host
+    function."""
+    return int(load().spec_anyorder_window(int(D), int(revealed), float(dtau)))
+
+
 class PreparedCall:
     """A C-ABI call with every argument marshalled once.  Calling it issues
     exactly one library call (no tensor allocation, no checks) on the stream
@@ -541,3 +612,21 @@ def prepare_anyorder(target_logits, draft_logits, order, draft_tokens, u_accept,
             _ptr(out_tokens), None, None, ws.data_ptr(), ws.numel(), sp)
     keep = (target_logits, draft_logits, order, draft_tokens, u_accept, u_sample, out_tokens, res, ws)
     return PreparedCall(lib.spec_verify_anyorder, args, keep, "spec_verify_anyorder")
+
+
+def prepare_rounds(target_logits, draft_logits, order, revealed, window, draft_tokens, u_accept,
+                   u_sample, out: RoundsResult,
+                   stream: Optional[torch.cuda.Stream] = None) -> PreparedCall:
+    """Validate once and return a PreparedCall repeating
+    spec_verify_anyorder_rounds on the same buffers."""
+    spec_verify_anyorder_rounds(target_logits, draft_logits, order, revealed, window, draft_tokens,
+                                u_accept, u_sample, out=out, stream=stream)
+    lib = load()
+    dev = target_logits.device
+    sp = _stream_ptr(stream, dev)
+    ws = get_workspace(256, dev, sp)
+    args = _rounds_args(target_logits, draft_logits, order, revealed, window, draft_tokens, u_accept,
+                        u_sample, out, ws, sp)
+    keep = (target_logits, draft_logits, order, revealed, window, draft_tokens, u_accept, u_sample,
+            out, ws)
+    return PreparedCall(lib.spec_verify_anyorder_rounds, args, keep, "spec_verify_anyorder_rounds")

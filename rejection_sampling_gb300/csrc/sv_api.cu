@@ -329,4 +329,61 @@ const char* spec_verify_status_string(int status) {
   }
 }
 
+
+int spec_verify_anyorder_rounds(const void* target_logits, const void* draft_logits,
+                                sv_dtype dtype, const int32_t* order, const int32_t* revealed,
+                                const int32_t* window, const int32_t* draft_tokens,
+                                const float* u_accept, const float* u_sample, int B, int R, int D,
+                                int V, int32_t* tokens, int32_t* n_revealed,
+                                int32_t* round_accepts, void* workspace, size_t ws_bytes,
+                                sv_stream_t stream) {
+  if (B < 0 || R < 1 || D < 1 || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
+  if ((long long)D * V > (1ll << 31) || (long long)B * R * D > (1ll << 31)) return SV_ERR_INVALID_ARG;
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !draft_logits || !order || !revealed || !window || !draft_tokens ||
+      !u_accept || !u_sample || !tokens || !n_revealed || !round_accepts || !workspace)
+    return SV_ERR_INVALID_ARG;
+  const int es = (dtype == SV_BF16) ? 2 : 4;
+  if (!aligned_to(target_logits, es) || !aligned_to(draft_logits, es)) return SV_ERR_INVALID_ARG;
+  const void* ptrs[] = {order, revealed, window, draft_tokens, u_accept, u_sample,
+                        tokens, n_revealed, round_accepts};
+  for (const void* q : ptrs)
+    if (!aligned_to(q, 4)) return SV_ERR_INVALID_ARG;
+  if (ws_bytes < sizeof(sv::WsHeader) || !aligned_to(workspace, 256)) return SV_ERR_INVALID_ARG;
+  sv::RoundsParams p;
+  memset(&p, 0, sizeof p);
+  p.lt = static_cast<const unsigned char*>(target_logits);
+  p.ld = static_cast<const unsigned char*>(draft_logits);
+  p.bf16 = dtype == SV_BF16;
+  p.order = order;
+  p.i0 = revealed;
+  p.win = window;
+  p.x = draft_tokens;
+  p.u_acc = u_accept;
+  p.u_s = u_sample;
+  p.B = B;
+  p.R = R;
+  p.D = D;
+  p.V = V;
+  p.tok_out = tokens;
+  p.n_out = n_revealed;
+  p.racc_out = round_accepts;
+  p.status = &reinterpret_cast<sv::WsHeader*>(workspace)->status;
+  return launch_status(sv::launch_rounds(p, (cudaStream_t)stream));
+}
+
+int spec_anyorder_window(int D, int revealed, float dtau) {
+  if (D < 1 || revealed < 0) return -1;
+  if (revealed >= D) return 0;
+  const double half_pi = 1.57079632679489661923;
+  // the schedule time at which `revealed` of D tokens are out: 1 - cos(t pi/2) = i/D
+  const double t = acos(1.0 - (double)revealed / (double)D) / half_pi;
+  const double t1 = fmin(1.0, t + (dtau > 0.f ? (double)dtau : 0.0));
+  long long end = (long long)ceil((double)D * (1.0 - cos(half_pi * t1)) - 1e-9);
+  if (end > D) end = D;
+  const long long w = end - revealed;
+  return (int)(w < 1 ? 1 : w);
+}
+
 }  // extern "C"

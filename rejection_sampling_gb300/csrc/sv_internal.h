@@ -159,6 +159,25 @@ cudaError_t launch_greedy(const DenseParams& p, cudaStream_t s);  // greedy: tar
 cudaError_t launch_commit(const DenseParams& p, float tau, int32_t* commit, float* confidence,
                           cudaStream_t s);
 // sparse support lists (temperature, top-k, top-p) from dense logits [N, V]
+// windowed multi-round any-order verification (one CTA per sequence)
+struct RoundsParams {
+  const unsigned char* lt;  // target logits [B, R, D, V]
+  const unsigned char* ld;  // draft logits [B, D, V]
+  int bf16;
+  const int32_t* order;     // sigma [B, D]
+  const int32_t* i0;        // revealed count [B]
+  const int32_t* win;       // window length [B]
+  const int32_t* x;         // draft tokens [B, R, D]
+  const float* u_acc;       // [B, R, D], by sigma index
+  const float* u_s;         // [B, R]
+  int B, R, D, V;
+  int32_t* tok_out;         // [B, D]
+  int32_t* n_out;           // [B]
+  int32_t* racc_out;        // [B, R]
+  uint32_t* status;
+};
+cudaError_t launch_rounds(const RoundsParams& p, cudaStream_t s);
+
 cudaError_t launch_support(const unsigned char* lt, int N, int V, int K, int bf16, int aligned,
                            float temperature, float top_p, int32_t* ids, float* probs,
                            uint32_t* status, cudaStream_t s);

@@ -298,6 +298,36 @@ def anyorder_inputs(B: int, D: int, W: int, V: int, *, dtype: str = "f32", seed:
                 u_accept=_uniform_f32(rng, (B, W)), u_sample=_uniform_f32(rng, (B,)))
 
 
+def rounds_inputs(B: int, R: int, D: int, V: int, *, dtype: str = "f32", seed: int = 0,
+                  draft_sigma: float = 2.0, target_noise: float = 0.4, wmax: int = 0) -> dict:
+    """Windowed multi-round any-order inputs.
+
+    draft [B, D, V] ~ N(0, draft_sigma^2) (one non-causal pass); target
+    [B, R, D, V] = draft + fresh N(0, target_noise^2) per round (the causal
+    recompute of each round); order [B, D] a random permutation per sequence;
+    revealed [B] uniform in [0, D); draft_tokens [B, R, D] sampled afresh per
+    round from the rounded draft logits; u_accept [B, R, D], u_sample [B, R].
+    With wmax > 0 also window [B] uniform in [1, wmax]; otherwise the caller
+    derives the windows (for instance from the cosine schedule).
+    """
+    rng = np.random.default_rng(seed)
+    ld = rng.normal(0.0, draft_sigma, size=(B, D, V)).astype(np.float32)
+    lt = (ld[:, None] + rng.normal(0.0, target_noise, size=(B, R, D, V))).astype(np.float32)
+    if dtype == "bf16":
+        lt, ld = bf16_bits(lt), bf16_bits(ld)
+    elif dtype != "f32":
+        raise ValueError(dtype)
+    order = np.stack([rng.permutation(D) for _ in range(B)]).astype(np.int32)
+    revealed = rng.integers(0, D, size=B).astype(np.int32)
+    tok = np.stack([gumbel_argmax(rng, ld, chunk_rows=8192) for _ in range(R)], axis=1).astype(np.int32)
+    d = dict(kind="rounds", dtype=dtype, B=B, R=R, D=D, V=V, target=np.ascontiguousarray(lt),
+             draft=ld, order=order, revealed=revealed, draft_tokens=np.ascontiguousarray(tok),
+             u_accept=_uniform_f32(rng, (B, R, D)), u_sample=_uniform_f32(rng, (B, R)))
+    if wmax > 0:
+        d["window"] = rng.integers(1, wmax + 1, size=B).astype(np.int32)
+    return d
+
+
 # ---------------------------------------------------------------------------
 # the five named workloads
 # ---------------------------------------------------------------------------
@@ -314,6 +344,10 @@ WORKLOADS = {
                                   target_sigma=3.0, draft_noise=0.5),
     "commit_b64_w4_v151936": dict(kind="commit", B=64, W=4, V=151936, dtype="bf16"),
     "support_b64_g7_v128256": dict(kind="support", B=64, gamma=7, V=128256, dtype="bf16"),
+    # text8-like character model (27 symbols), 256 positions, 4 verification
+    # rounds per draft, windows from the cosine schedule with dtau = 0.05
+    "rounds_b4096_r4_d256_v27": dict(kind="rounds", B=4096, R=4, D=256, V=27, dtype="f32",
+                                     dtau=0.05),
 }
 
 
@@ -342,6 +376,11 @@ def make(name: str, seed: int = 0, **override) -> dict:
         rows = np.concatenate([dd["target"].reshape(-1, V), dd["draft"].reshape(-1, V)])
         d = dict(kind="support", dtype=dd["dtype"], N=rows.shape[0], V=V, K=50, T=1.0,
                  top_p=0.95, logits=np.ascontiguousarray(rows))
+    elif kind == "rounds":
+        dtau = cfg.pop("dtau")
+        B, R, D, V = cfg.pop("B"), cfg.pop("R"), cfg.pop("D"), cfg.pop("V")
+        d = rounds_inputs(B, R, D, V, seed=seed, **cfg)
+        d["dtau"] = dtau  # the windows come from the cosine schedule (computed by the caller)
     else:
         B, D, W, V = cfg.pop("B"), cfg.pop("D"), cfg.pop("W"), cfg.pop("V")
         d = anyorder_inputs(B, D, W, V, seed=seed, **cfg)
