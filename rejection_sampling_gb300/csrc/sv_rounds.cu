@@ -10,8 +10,15 @@
 // and the next round starts after it.  A round that accepts every remaining
 // draft closes the window; there is no bonus token.
 //
-// Design: one CTA of 8 warps per sequence, every round in one launch.  A round
-// takes its positions eight at a time, one warp per position: the warp reads
+// Design, vocabularies up to 512 (rounds_lane_kernel): one warp per sequence,
+// every round in one launch; lane j takes window slot j of the current group
+// of 32, forms its rows' statistics alone and keeps its draft statistics in
+// registers; a ballot finds the round's first position that is not accepted,
+// so nothing synchronises the block.
+//
+// Design, larger vocabularies (rounds_kernel): one CTA of 8 warps per
+// sequence, every round in one launch.  A round takes its positions eight at
+// a time, one warp per position: the warp reads
 // the target row, forms its softmax statistics (c = log2e * max, S in
 // float-float) and the accept probability at its draft token (the same
 // arithmetic as the single-round kernels); the draft row's statistics are
@@ -28,6 +35,7 @@ namespace {
 constexpr int kRWarps = 8;
 constexpr int kRThreads = 32 * kRWarps;
 constexpr int kDraftCache = 1024;  // window positions whose draft statistics are kept
+constexpr int kLaneMaxV = 512;     // vocabularies a lane reduces alone
 
 __device__ __forceinline__ float logit_at(const unsigned char* row, int y, int bf16) {
   if (bf16) return bf16_to_f32(reinterpret_cast<const uint16_t*>(row)[y]);
@@ -239,10 +247,147 @@ __global__ void __launch_bounds__(kRThreads) rounds_kernel(const __grid_constant
   if (tid == 0) P.n_out[b] = i;
 }
 
+// softmax statistics of one logit row, one lane alone (small vocabularies):
+// the same quantities as row_stats_global, float-float sum
+__device__ __forceinline__ Stats row_stats_lane(const unsigned char* row, int V, int bf16) {
+  float m = -INFINITY;
+  int odd = 0;
+  for (int y = 0; y < V; ++y) {
+    const float v = logit_at(row, y, bf16);
+    odd |= (v != v) || (v == INFINITY);
+    m = fmaxf(m, v);
+  }
+  const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
+  ff a0{0.f, 0.f}, a1{0.f, 0.f};
+  int y = 0;
+  for (; y + 1 < V; y += 2) {
+    a0 = ff_add_f(a0, ex2(fmaf(logit_at(row, y, bf16), kLog2e, -c)));
+    a1 = ff_add_f(a1, ex2(fmaf(logit_at(row, y + 1, bf16), kLog2e, -c)));
+  }
+  if (y < V) a0 = ff_add_f(a0, ex2(fmaf(logit_at(row, y, bf16), kLog2e, -c)));
+  Stats s;
+  s.S = ff_to_f(ff_add(a0, a1));
+  s.c = (m == -INFINITY) ? -INFINITY : c;
+  s.bad = odd || !(m > -INFINITY) || !(s.S > 0.f) || !(s.S < INFINITY);
+  return s;
+}
+
+// Small vocabularies: one warp per sequence, lane j on window slot j of the
+// current group of 32 (sigma index i0 + 32 g + j).  Each active lane forms its
+// rows' statistics alone (the draft row's once, kept in registers for the
+// first group); a ballot gives the first position that is not accepted, so a
+// round needs no block barrier; the whole warp then draws.
+__global__ void __launch_bounds__(kRThreads) rounds_lane_kernel(const __grid_constant__ RoundsParams P) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * kRWarps + (threadIdx.x >> 5);
+  if (b >= P.B) return;  // whole warps only: nothing below synchronises the block
+  const int R = P.R, D = P.D, V = P.V;
+  const size_t es = P.bf16 ? 2 : 4;
+  const int32_t* sig = P.order + (size_t)b * D;
+  int32_t* out = P.tok_out + (size_t)b * D;
+  int32_t* racc = P.racc_out + (size_t)b * R;
+  const int i0 = P.i0[b], W = P.win[b];
+  int bad = (i0 < 0 || i0 > D || W < 1);
+  const int e = bad ? 0 : ((W > D - i0) ? D : i0 + W);
+  int odd = 0;
+  for (int k = i0 + lane; k < e; k += 32) {
+    const int s = sig[k];
+    odd |= (s < 0 || s >= D);
+    for (int k2 = i0; k2 < k && !odd; ++k2) odd |= (sig[k2] == s);
+  }
+  for (int r = lane; r < R; r += 32) racc[r] = -1;
+  bad |= __any_sync(0xffffffffu, odd);
+  __syncwarp();
+
+  Stats dcache;  // the draft statistics of this lane's slot in group 0
+  int have = 0;
+  int i = i0;
+  for (int r = 0; r < R; ++r) {
+    if (bad || i >= e) break;  // warp-uniform
+    const size_t rr = ((size_t)b * R + r) * (size_t)D;
+    int stop = e, err = 0;
+    Stats st{0.f, 1.f, 0}, sd{0.f, 1.f, 0};  // the stop position's statistics
+    for (int g = (i - i0) >> 5; i0 + 32 * g < e; ++g) {
+      const int k = i0 + 32 * g + lane;
+      const bool active = (k >= i) && (k < e);
+      int res = 0;
+      Stats t{0.f, 1.f, 0}, d{0.f, 1.f, 0};
+      if (active) {
+        const int s = sig[k];
+        const int x = P.x[rr + s];
+        const unsigned char* trow = P.lt + (rr + s) * (size_t)V * es;
+        const unsigned char* drow = P.ld + ((size_t)b * D + s) * (size_t)V * es;
+        t = row_stats_lane(trow, V, P.bf16);
+        if (g == 0 && have) {
+          d = dcache;
+        } else {
+          d = row_stats_lane(drow, V, P.bf16);
+          if (g == 0) {
+            dcache = d;
+            have = 1;
+          }
+        }
+        res = 2;
+        if (!t.bad && !d.bad && x >= 0 && x < V) {
+          const float a = accept_prob(logit_at(trow, x, P.bf16), logit_at(drow, x, P.bf16), t, d);
+          res = (P.u_acc[rr + k] < a) ? 0 : 1;
+        }
+      }
+      const unsigned nacc = __ballot_sync(0xffffffffu, active && res != 0);
+      if (nacc) {
+        const int j = __ffs(nacc) - 1;
+        stop = i0 + 32 * g + j;
+        err = __shfl_sync(0xffffffffu, res, j) == 2;
+        st.c = __shfl_sync(0xffffffffu, t.c, j);
+        st.S = __shfl_sync(0xffffffffu, t.S, j);
+        sd.c = __shfl_sync(0xffffffffu, d.c, j);
+        sd.S = __shfl_sync(0xffffffffu, d.S, j);
+        break;
+      }
+    }
+    if (err) {
+      bad = 1;
+      break;
+    }
+    for (int k = i + lane; k < stop; k += 32) out[sig[k]] = P.x[rr + sig[k]];
+    if (lane == 0) racc[r] = stop - i;
+    if (stop < e) {
+      const int s = sig[stop];
+      const unsigned char* trow = P.lt + (rr + s) * (size_t)V * es;
+      const unsigned char* drow = P.ld + ((size_t)b * D + s) * (size_t)V * es;
+      const int y = warp_draw(trow, drow, V, P.bf16, st.c, st.S, sd.c, sd.S, P.u_s[(size_t)b * R + r], lane);
+      if (lane == 0) out[s] = y;
+      i = stop + 1;
+    } else {
+      i = e;
+    }
+    __syncwarp();
+  }
+
+  if (bad) {
+    __syncwarp();
+    for (int k = (i0 > 0 ? i0 : 0) + lane; k < e; k += 32) {
+      const int s = sig[k];
+      if (s >= 0 && s < D) out[s] = -1;
+    }
+    for (int r = lane; r < R; r += 32) racc[r] = -1;
+    if (lane == 0) {
+      P.n_out[b] = -1;
+      atomicOr(P.status, kStatusInputErr);
+    }
+    return;
+  }
+  if (lane == 0) P.n_out[b] = i;
+}
+
 }  // namespace
 
 cudaError_t launch_rounds(const RoundsParams& p, cudaStream_t s) {
-  rounds_kernel<<<p.B, kRThreads, 0, s>>>(p);
+  if (p.V <= kLaneMaxV) {  // a lane per window position, a warp per sequence
+    rounds_lane_kernel<<<(p.B + kRWarps - 1) / kRWarps, kRThreads, 0, s>>>(p);
+  } else {  // a warp per window position, a CTA per sequence
+    rounds_kernel<<<p.B, kRThreads, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 

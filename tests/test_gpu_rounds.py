@@ -64,6 +64,8 @@ def rounds_parity(d, window, min_clean=0.9):
     (6, 2, 20, 50000, "bf16", 12),    # a large vocabulary
     (40, 1, 16, 7, "f32", 16),        # one round
     (8, 6, 9, 2, "f32", 9),           # two symbols, many rounds
+    (12, 3, 24, 512, "bf16", 24),     # the largest vocabulary a lane reduces alone
+    (12, 3, 24, 513, "f32", 24),      # the smallest one a warp reduces per position
 ])
 def test_rounds_parity(B, R, D, V, dtype, wmax):
     d = wl.rounds_inputs(B, R, D, V, dtype=dtype, seed=B + R + D + V % 97, wmax=wmax)
@@ -77,14 +79,17 @@ def test_rounds_cosine_windows_text8_like():
     assert (racc[:, 0] >= 0).all()  # every window has at least one position
 
 
-def test_rounds_long_windows_past_the_draft_cache():
-    # windows of up to 1500 positions: groups of eight, cached draft statistics
-    # for the first 1024 window positions, recomputed beyond
-    d = wl.rounds_inputs(4, 3, 1500, 5, dtype="f32", seed=11, target_noise=1e-3)
-    d["revealed"][:] = [0, 0, 100, 1499]
-    window = np.array([1500, 1200, 1400, 1], np.int32)
+@pytest.mark.parametrize("V,D", [(5, 1500), (600, 1200)])
+def test_rounds_long_windows(V, D):
+    # windows of more than a thousand positions: for small vocabularies groups
+    # of 32 lanes (draft statistics kept for the first group only), for large
+    # ones groups of eight warps (draft statistics kept for the first 1024
+    # window positions); a near-identical target runs deep into the window
+    d = wl.rounds_inputs(4, 3, D, V, dtype="f32", seed=11, target_noise=1e-3)
+    d["revealed"][:] = [0, 0, 100, D - 1]
+    window = np.array([D, D - 300, D - 100, 1], np.int32)
     tok, n, racc, o = rounds_parity(d, window, min_clean=0.5)
-    assert n.max() > 1024  # the near-identical target runs past the cached positions
+    assert n.max() > 1024
 
 
 def test_rounds_input_errors():
