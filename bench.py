@@ -230,6 +230,7 @@ def variant_lines(dev, stream):
                 args = [t.clone() for t in base]
                 o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_dense(*args, out=o, stream=stream))
         elif d["kind"] == "greedy":
             B, G, V = d["B"], d["gamma"], d["V"]
@@ -241,6 +242,7 @@ def variant_lines(dev, stream):
                 args = [t.clone() for t in base]
                 o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_greedy(*args, out=o, stream=stream))
         elif d["kind"] == "commit":
             B, W, V = d["B"], d["W"], d["V"]
@@ -253,6 +255,7 @@ def variant_lines(dev, stream):
                 args = [t.clone() for t in base]
                 o = rs.CommitResult(torch.empty(B, W, dtype=torch.int32, device=dev),
                                     torch.empty(B, W, dtype=torch.int32, device=dev), None)
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_commit(*args, d["tau"], out=o, stream=stream))
         elif d["kind"] == "support":
             N, V, K = d["N"], d["V"], d["K"]
@@ -264,6 +267,7 @@ def variant_lines(dev, stream):
                 lg = base.clone()
                 o = rs.SupportResult(torch.empty(N, K, dtype=torch.int32, device=dev),
                                      torch.empty(N, K, dtype=torch.float32, device=dev))
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_support(lg, d["T"], K, d["top_p"], out=o, stream=stream))
         elif d["kind"] == "rounds":
             B, R, D, V = d["B"], d["R"], d["D"], d["V"]
@@ -277,6 +281,7 @@ def variant_lines(dev, stream):
                 o = rs.RoundsResult(torch.full((B, D), -1, dtype=torch.int32, device=dev),
                                     torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, R, dtype=torch.int32, device=dev))
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_rounds(*args, out=o, stream=stream))
             torch.cuda.synchronize()
             revealed = int((o.n_revealed - base[3]).sum())
@@ -293,6 +298,7 @@ def variant_lines(dev, stream):
                 args = [t.clone() for t in base]
                 o = rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None)
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
                 calls.append(rs.prepare_sparse(*args, d["V"], out=o, stream=stream))
         else:
             B, D, W, V = d["B"], d["D"], d["W"], d["V"]
@@ -302,8 +308,9 @@ def variant_lines(dev, stream):
                                                 "u_accept", "u_sample")]
             for c in range(copies):
                 args = [t.clone() for t in base]
-                calls.append(rs.prepare_anyorder(*args, torch.full((B, D), -1, dtype=torch.int32,
-                                                                   device=dev), stream=stream))
+                tok = torch.full((B, D), -1, dtype=torch.int32, device=dev)
+                torch.cuda.synchronize()  # inputs built on the default stream; calls run on `stream`
+                calls.append(rs.prepare_anyorder(*args, tok, stream=stream))
         with torch.cuda.stream(stream):
             ms = time_prepared(calls, stream, 400)
         out[name] = {"us_per_call": round(ms * 1e3, 2),
@@ -365,6 +372,7 @@ def run_ours(args):
         sets.append([t.clone() for t in base] if c else base)
         outs.append(rs.VerifyResult(torch.empty(B, dtype=torch.int32, device=dev),
                                     torch.empty(B, G + 1, dtype=torch.int32, device=dev), None, None))
+    torch.cuda.synchronize()  # the copies are built on the default stream; the calls run on `stream`
     calls = [rs.prepare_dense(*sets[c], out=outs[c], stream=stream) for c in range(2)]
     torch.cuda.synchronize()
 
@@ -419,8 +427,8 @@ def run_ours(args):
         pin = {k: torch.from_numpy(np.ascontiguousarray(v)).pin_memory() for k, v in host.items()}
         pin["target"] = pin["target"].view(torch.bfloat16)
         pin["draft"] = pin["draft"].view(torch.bfloat16)
-        dst = [torch.empty_like(pin[k], device=dev) for k in ("target", "draft", "draft_ids",
-                                                                "u_accept", "u_sample")]
+        dst = [pin[k].to(dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
+        torch.cuda.synchronize()  # the validating call below runs on `stream`
         o = outs[0]
         call = rs.prepare_dense(*dst, out=o, stream=stream)
         h_n = torch.empty(B, dtype=torch.int32).pin_memory()
@@ -545,8 +553,8 @@ def run_reference(args):
 
 def run_calls_only(args):
     """Profiling driver: args.calls_only untimed calls of one workload (the
-    headline by default; ``--workload NAME`` for the greedy, commit and
-    support paths), no output beyond one status line (ncu's launch filters pick the
+    headline by default; ``--workload NAME`` for the greedy, commit, support
+    and rounds paths), no output beyond one status line (ncu's launch filters pick the
     kernels out)."""
     import torch
     import rejection_sampling_gb300 as rs
@@ -568,8 +576,16 @@ def run_calls_only(args):
     elif d["kind"] == "support":
         t = [to_dev(d["logits"], dev), d["T"], d["K"], d["top_p"]]
         fn = rs.spec_support_topk
+    elif d["kind"] == "rounds":
+        import numpy as np
+        window = np.array([rs.spec_anyorder_window(d["D"], int(i), d["dtau"]) for i in d["revealed"]],
+                          np.int32)
+        t = [to_dev(x, dev) for x in (d["target"], d["draft"], d["order"], d["revealed"], window,
+                                      d["draft_tokens"], d["u_accept"], d["u_sample"])]
+        fn = rs.spec_verify_anyorder_rounds
     else:
-        raise SystemExit(f"--calls-only drives dense, greedy, commit and support workloads, not {name}")
+        raise SystemExit(f"--calls-only drives dense, greedy, commit, support and rounds workloads, "
+                         f"not {name}")
     for _ in range(args.calls_only):
         fn(*t)
     torch.cuda.synchronize()
