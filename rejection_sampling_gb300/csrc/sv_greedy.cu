@@ -372,18 +372,24 @@ __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __gri
 // are committed, and when none clears tau the most confident one is (the
 // smallest index on ties), so every pass makes progress.
 //  * commit_stats_kernel: the greedy statistics kernel's sweep over the
-//    logits [B, W, V] (pieces of positions no longer masked are skipped),
-//    adding per piece S = sum 2^((v - m) log2e) (ex2.approx) to (max, first
-//    id, bad); segments fold (m, S) with one rescale (float-float).
+//    logits [B, W, V], only over the pieces of masked positions: each CTA
+//    lists the masked positions (a block-wide compaction of the flags, for
+//    up to 8192 positions; beyond that every piece is swept and unmasked
+//    ones are skipped) and the warps take equal shares of their pieces.  Per
+//    piece S = sum 2^((v - m) log2e) (ex2.approx) joins (max, first id, bad);
+//    segments fold (m, S) with one rescale (float-float) and leave a marked
+//    record at their first piece's slot.
 //  * commit_row_kernel: one CTA per block; a warp per masked position
-//    combines its records into (c_i, a_i); thread 0 applies the threshold.
+//    collects the marked records in its position's slots into (c_i, a_i)
+//    and zeroes them; thread 0 applies the threshold.
 // ---------------------------------------------------------------------------
 struct ConfRec {  // one segment (32 bytes, at the segment's first piece slot)
   float m;        // maximum
   float s_hi, s_lo;  // sum 2^((v - m) log2e), float-float
   int idx;        // first id holding the maximum
   int bad;        // a NaN or +inf was seen
-  int pad[3];
+  int live;       // 1: a record is here (the workspace is zero elsewhere)
+  int pad[2];
 };
 
 struct CSeg {
@@ -399,7 +405,44 @@ __device__ __forceinline__ bool is_masked(const DenseParams& P, int b, int j) {
   return __ldg(P.x + (size_t)b * (P.G + 1) + j) != 0;
 }
 
-__device__ __forceinline__ void cseg_begin(CSeg& s, const DenseParams& P, const GItem& it, long long w) {
+constexpr int kCMaxList = 8192;  // positions whose masked subset is listed in shared memory
+
+// Pieces in the order the statistics warps sweep them: every piece of the
+// batch (all = 1), or only the pieces of masked positions, position list[m]
+// for m = 0, 1, ... (all = 0), so that the warps' shares hold equal work.
+struct CItem {
+  int b, j, k, m;
+};
+__device__ __forceinline__ CItem citem_at(long long q, int all, const int* list, int Wn, int np) {
+  CItem it;
+  const long long r = q / np;
+  it.k = (int)(q - r * np);
+  const int pos = all ? (int)r : list[r];
+  it.m = (int)r;
+  it.b = pos / Wn;
+  it.j = pos - it.b * Wn;
+  return it;
+}
+__device__ __forceinline__ void citem_next(CItem& it, int all, const int* list, int M, int Wn, int np) {
+  if (++it.k < np) return;
+  it.k = 0;
+  ++it.m;
+  if (all) {
+    if (++it.j == Wn) {
+      it.j = 0;
+      ++it.b;
+    }
+  } else if (it.m < M) {
+    it.b = list[it.m] / Wn;
+    it.j = list[it.m] - it.b * Wn;
+  }
+}
+// the record slot of a piece: its index among all pieces of the batch
+__device__ __forceinline__ long long citem_slot(const CItem& it, int Wn, int np) {
+  return ((long long)it.b * Wn + it.j) * np + it.k;
+}
+
+__device__ __forceinline__ void cseg_begin(CSeg& s, const DenseParams& P, const CItem& it, long long w) {
   s.w0 = w;
   s.b = it.b;
   s.j = it.j;
@@ -413,12 +456,12 @@ __device__ __forceinline__ void cseg_write(const DenseParams& P, const CSeg& s, 
   if (lane == 0 && s.live) {
     int4* q = reinterpret_cast<int4*>(reinterpret_cast<ConfRec*>(P.ws + P.L.upart) + s.w0);
     q[0] = make_int4(__float_as_int(s.m), __float_as_int(s.S.hi), __float_as_int(s.S.lo), s.idx);
-    q[1] = make_int4(s.bad, 0, 0, 0);
+    q[1] = make_int4(s.bad, 1, 0, 0);  // .y = 1 marks a record
   }
 }
 // (max, sum, first id, bad) of a piece folded into the segment (pieces in
 // increasing id order: a strictly greater maximum takes over, ties keep it)
-__device__ __forceinline__ void cseg_add(CSeg& s, const GItem& it, const uint4 (&r)[4], int bf16,
+__device__ __forceinline__ void cseg_add(CSeg& s, const CItem& it, const uint4 (&r)[4], int bf16,
                                          int pe, int lane) {
   float m;
   int idx, bad;
@@ -451,10 +494,41 @@ __device__ __forceinline__ void cseg_add(CSeg& s, const GItem& it, const uint4 (
 
 __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ int s_list[kCMaxList];
+  __shared__ int s_wsum[kGWarps];
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int G = P.G, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
-  const long long W = (long long)P.B * (G + 1) * np;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = P.G, Wn = G + 1, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
+  const int npos = P.B * Wn;
+  // the masked positions in order (a block-wide compaction of the flags)
+  const int all = npos > kCMaxList;
+  int M = npos;
+  if (!all) {
+    const int C = (npos + kGThreads - 1) / kGThreads;
+    const int p0 = min(npos, tid * C), p1 = min(npos, p0 + C);
+    int cnt = 0;
+    for (int p = p0; p < p1; ++p) cnt += (__ldg(P.x + p) != 0);
+    int incl = cnt;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    int base = 0;
+    M = 0;
+    for (int w2 = 0; w2 < kGWarps; ++w2) {
+      const int v = s_wsum[w2];
+      if (w2 < warp) base += v;
+      M += v;
+    }
+    int o = base + incl - cnt;
+    for (int p = p0; p < p1; ++p)
+      if (__ldg(P.x + p) != 0) s_list[o++] = p;
+    __syncthreads();
+  }
+  const long long W = (long long)M * np;
   const long long nwt = (long long)gridDim.x * kGWarps;
   const long long gw = (long long)blockIdx.x * kGWarps + warp;
   const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
@@ -462,14 +536,14 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
   if (lo >= hi) return;
   const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
   CSeg seg;
-  GItem out = gitem_at(lo, G, np);
-  cseg_begin(seg, P, out, lo);
+  CItem out = citem_at(lo, all, s_list, Wn, np);
+  cseg_begin(seg, P, out, citem_slot(out, Wn, np));
 
   if (!P.aligned) {
-    for (long long w = lo; w < hi; ++w, gitem_next(out, G, np)) {
+    for (long long w = lo; w < hi; ++w, citem_next(out, all, s_list, M, Wn, np)) {
       if (out.b != seg.b || out.j != seg.j) {
         cseg_write(P, seg, lane);
-        cseg_begin(seg, P, out, w);
+        cseg_begin(seg, P, out, citem_slot(out, Wn, np));
       }
       if (!seg.live) continue;
       const int ne = min(pe, P.V - out.k * pe);
@@ -482,7 +556,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
   }
 
   unsigned char* ring = smem_raw + (size_t)warp * kGStages * kPieceBytes;
-  GItem in = out;
+  CItem in = out;
   long long wi = lo;
   auto issue = [&](int s) {  // pieces of positions no longer masked are not read
     if (!is_masked(P, in.b, in.j)) return;
@@ -498,7 +572,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
   for (int s = 0; s < kGStages - 1; ++s) {
     if (wi < hi) {
       issue(s);
-      gitem_next(in, G, np);
+      citem_next(in, all, s_list, M, Wn, np);
       ++wi;
     }
     cp_async_commit();
@@ -507,11 +581,11 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
   for (long long w = lo; w < hi; ++w) {
     if (out.b != seg.b || out.j != seg.j) {
       cseg_write(P, seg, lane);
-      cseg_begin(seg, P, out, w);
+      cseg_begin(seg, P, out, citem_slot(out, Wn, np));
     }
     if (wi < hi) {
       issue(islot);
-      gitem_next(in, G, np);
+      citem_next(in, all, s_list, M, Wn, np);
       ++wi;
     }
     cp_async_commit();
@@ -528,7 +602,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
       }
       cseg_add(seg, out, r, P.bf16, pe, lane);
     }
-    gitem_next(out, G, np);
+    citem_next(out, all, s_list, M, Wn, np);
     slot = (slot + 1 == kGStages) ? 0 : slot + 1;
     islot = (islot + 1 == kGStages) ? 0 : islot + 1;
   }
@@ -548,7 +622,6 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   ConfRec* rec = reinterpret_cast<ConfRec*>(P.ws + P.L.upart);
-  const long long W = (long long)P.B * Wn * np, nwt = P.stats_warps;
   for (int j = warp; j < Wn; j += kGRowWarps) {
     const bool masked = P.x[(size_t)b * Wn + j] != 0;
     if (!masked) {  // no record was written for it
@@ -558,16 +631,17 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
       }
       continue;
     }
-    const long long P0 = ((long long)b * Wn + j) * np, P1 = P0 + np;
-    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    // the position's records sit at the first piece of each segment that
+    // covers it, marked; every other slot of its range is zero
+    const long long P0 = ((long long)b * Wn + j) * np;
     float m = -INFINITY;
     ff S{0.f, 0.f};
     int idx = INT_MAX, bad = 0;
-    for (long long g = g0 + lane; g <= g1; g += 32) {
-      const long long l0 = g * W / nwt, l1 = (g + 1) * W / nwt;
-      if (l1 <= l0) continue;
-      int4* rp = reinterpret_cast<int4*>(rec + (l0 > P0 ? l0 : P0));
-      const int4 v0 = __ldcg(rp), v1 = __ldcg(rp + 1);
+    for (int k = lane; k < np; k += 32) {
+      int4* rp = reinterpret_cast<int4*>(rec + P0 + k);
+      const int4 v1 = __ldcg(rp + 1);
+      if (v1.y != 1) continue;
+      const int4 v0 = __ldcg(rp);
       rp[0] = make_int4(0, 0, 0, 0);
       rp[1] = make_int4(0, 0, 0, 0);
       bad |= v1.x;
