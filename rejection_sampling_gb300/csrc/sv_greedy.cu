@@ -637,24 +637,35 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
     float m = -INFINITY;
     ff S{0.f, 0.f};
     int idx = INT_MAX, bad = 0;
-    for (int k = lane; k < np; k += 32) {
-      int4* rp = reinterpret_cast<int4*>(rec + P0 + k);
-      const int4 v1 = __ldcg(rp + 1);
-      if (v1.y != 1) continue;
-      const int4 v0 = __ldcg(rp);
-      rp[0] = make_int4(0, 0, 0, 0);
-      rp[1] = make_int4(0, 0, 0, 0);
-      bad |= v1.x;
-      const float rm = __int_as_float(v0.x);
-      const ff rs{__int_as_float(v0.y), __int_as_float(v0.z)};
-      if (rm == -INFINITY) continue;
-      if (rm > m) {
-        S = ff_add(ff_mul_f(S, (m == -INFINITY) ? 0.f : exp2f((m - rm) * kLog2e)), rs);
-        m = rm;
-        idx = v0.w;
-      } else {
-        S = ff_add(S, ff_mul_f(rs, exp2f((rm - m) * kLog2e)));
-        if (rm == m && v0.w < idx) idx = v0.w;
+    for (int k0 = lane; k0 < np; k0 += 4 * 32) {  // four slots per lane in flight at once
+      int4 v0[4], v1[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v1[u] = make_int4(0, 0, 0, 0);
+        if (k0 + 32 * u < np) {
+          const int4* rp = reinterpret_cast<const int4*>(rec + P0 + k0 + 32 * u);
+          v0[u] = __ldcg(rp);
+          v1[u] = __ldcg(rp + 1);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (v1[u].y != 1) continue;
+        int4* rp = reinterpret_cast<int4*>(rec + P0 + k0 + 32 * u);
+        rp[0] = make_int4(0, 0, 0, 0);
+        rp[1] = make_int4(0, 0, 0, 0);
+        bad |= v1[u].x;
+        const float rm = __int_as_float(v0[u].x);
+        const ff rs{__int_as_float(v0[u].y), __int_as_float(v0[u].z)};
+        if (rm == -INFINITY) continue;
+        if (rm > m) {
+          S = ff_add(ff_mul_f(S, (m == -INFINITY) ? 0.f : exp2f((m - rm) * kLog2e)), rs);
+          m = rm;
+          idx = v0[u].w;
+        } else {
+          S = ff_add(S, ff_mul_f(rs, exp2f((rm - m) * kLog2e)));
+          if (rm == m && v0[u].w < idx) idx = v0[u].w;
+        }
       }
     }
     // warp: rescale every lane's sum to the warp maximum, then add
