@@ -479,6 +479,10 @@ __global__ void __launch_bounds__(32 * W, 3)
   __shared__ float s_lv[W][32];
   __shared__ float s_thr;
   __shared__ int s_bad, s_gcnt;
+  // a programmatic dependent of whatever precedes it on the stream: nothing is
+  // read before that grid has completed; the next call may launch at once
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int row = blockIdx.x, V = P.V, K = P.K;
   const size_t es = P.bf16 ? 2 : 4;
@@ -728,11 +732,20 @@ cudaError_t launch_support(const unsigned char* lt, int N, int V, int K, int bf1
     if (e != cudaSuccess) return e;
     attr[dev] = true;
   }
-  if (K <= 32) support_kernel<1, 8><<<N, 256, ring, s>>>(p);
-  else if (K <= 64) support_kernel<2, 8><<<N, 256, ring, s>>>(p);
-  else if (K <= 128) support_kernel<4, 8><<<N, 256, ring, s>>>(p);
-  else support_kernel<8, 8><<<N, 256, ring, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute pdl[1];  // launched as a programmatic dependent (see the kernel)
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)N, 1, 1);
+  cfg.blockDim = dim3(256, 1, 1);
+  cfg.dynamicSmemBytes = ring;
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (K <= 32) return cudaLaunchKernelEx(&cfg, support_kernel<1, 8>, p);
+  if (K <= 64) return cudaLaunchKernelEx(&cfg, support_kernel<2, 8>, p);
+  if (K <= 128) return cudaLaunchKernelEx(&cfg, support_kernel<4, 8>, p);
+  return cudaLaunchKernelEx(&cfg, support_kernel<8, 8>, p);
 }
 
 }  // namespace sv
