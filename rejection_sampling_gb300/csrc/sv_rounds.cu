@@ -272,13 +272,49 @@ __device__ __forceinline__ Stats row_stats_lane(const unsigned char* row, int V,
   return s;
 }
 
+// The same statistics for an fp32 row of at most 32 logits: the lane copies
+// its row into its own shared-memory slot with independent 4-byte cp.async
+// copies (one round trip instead of a chain of loads), then reduces it there;
+// a slot stride of 33 floats keeps the lanes of a warp in distinct banks.
+__device__ __forceinline__ Stats row_stats_lane_staged(const unsigned char* row, int V, float* slot) {
+  const float* g = reinterpret_cast<const float*>(row);
+  for (int y = 0; y < V; ++y)
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(slot + y)), "l"(g + y)
+                 : "memory");
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
+  float m = -INFINITY;
+  int odd = 0;
+  for (int y = 0; y < V; ++y) {
+    const float v = slot[y];
+    odd |= (v != v) || (v == INFINITY);
+    m = fmaxf(m, v);
+  }
+  const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
+  ff a0{0.f, 0.f}, a1{0.f, 0.f};
+  int y = 0;
+  for (; y + 1 < V; y += 2) {
+    a0 = ff_add_f(a0, ex2(fmaf(slot[y], kLog2e, -c)));
+    a1 = ff_add_f(a1, ex2(fmaf(slot[y + 1], kLog2e, -c)));
+  }
+  if (y < V) a0 = ff_add_f(a0, ex2(fmaf(slot[y], kLog2e, -c)));
+  Stats s;
+  s.S = ff_to_f(ff_add(a0, a1));
+  s.c = (m == -INFINITY) ? -INFINITY : c;
+  s.bad = odd || !(m > -INFINITY) || !(s.S > 0.f) || !(s.S < INFINITY);
+  return s;
+}
+
 // Small vocabularies: one warp per sequence, lane j on window slot j of the
 // current group of 32 (sigma index i0 + 32 g + j).  Each active lane forms its
 // rows' statistics alone (the draft row's once, kept in registers for the
 // first group); a ballot gives the first position that is not accepted, so a
 // round needs no block barrier; the whole warp then draws.
 __global__ void __launch_bounds__(kRThreads) rounds_lane_kernel(const __grid_constant__ RoundsParams P) {
+  __shared__ float s_rowbuf[kRWarps * 32 * 33];
   const int lane = threadIdx.x & 31;
+  float* const rslot = s_rowbuf + (threadIdx.x >> 5) * 32 * 33 + lane * 33;
+  const bool staged = !P.bf16 && P.V <= 32;  // fp32 rows short enough to stage
   const int b = blockIdx.x * kRWarps + (threadIdx.x >> 5);
   if (b >= P.B) return;  // whole warps only: nothing below synchronises the block
   const int R = P.R, D = P.D, V = P.V;
@@ -317,11 +353,11 @@ __global__ void __launch_bounds__(kRThreads) rounds_lane_kernel(const __grid_con
         const int x = P.x[rr + s];
         const unsigned char* trow = P.lt + (rr + s) * (size_t)V * es;
         const unsigned char* drow = P.ld + ((size_t)b * D + s) * (size_t)V * es;
-        t = row_stats_lane(trow, V, P.bf16);
+        t = staged ? row_stats_lane_staged(trow, V, rslot) : row_stats_lane(trow, V, P.bf16);
         if (g == 0 && have) {
           d = dcache;
         } else {
-          d = row_stats_lane(drow, V, P.bf16);
+          d = staged ? row_stats_lane_staged(drow, V, rslot) : row_stats_lane(drow, V, P.bf16);
           if (g == 0) {
             dcache = d;
             have = 1;
