@@ -237,3 +237,34 @@ def test_unreached_rows_are_not_read(oracle_mod):
     o = oracle_mod.anyorder_rounds(lt, ld, order, [0], [D], x, ua, us)
     assert o["round_accepts"].tolist() == [[1]] and o["n_revealed"].tolist() == [2]
     assert o["flags"][0] & 8 == 0
+
+
+def test_round_bookkeeping_invariants(oracle_mod):
+    # on random inputs: each round reveals its accepted drafts plus, unless it
+    # closed the window, the resampled position; the revealed positions are
+    # exactly sigma[i0, n); nothing else changes; the rounds run form a prefix
+    rng = np.random.default_rng(9)
+    B, R, D, V = 200, 5, 24, 6
+    lt, ld, order, x, ua, us = _case(rng, B, R, D, V, noise=1.0)
+    i0 = rng.integers(0, D + 1, size=B).astype(np.int32)
+    win = rng.integers(1, D + 3, size=B).astype(np.int32)
+    init = np.full((B, D), -5, np.int32)
+    o = oracle_mod.anyorder_rounds(lt, ld, order, i0, win, x, ua, us, tokens_init=init)
+    assert (o["n_revealed"] >= 0).all()
+    for b in range(B):
+        e = min(D, int(i0[b]) + int(win[b]))
+        ra = o["round_accepts"][b]
+        ran = ra >= 0
+        assert (np.diff(ran.astype(int)) <= 0).all()  # a prefix of the rounds ran
+        i = int(i0[b])
+        for r in np.nonzero(ran)[0]:
+            i += int(ra[r]) + (1 if i + int(ra[r]) < e else 0)
+            assert i <= e
+        assert i == o["n_revealed"][b]
+        assert (i == e) or ran.all()  # stopped early only by closing the window
+        revealed = set(order[b, i0[b]:i].tolist())
+        for pos in range(D):
+            if pos in revealed:
+                assert 0 <= o["tokens"][b, pos] < V
+            else:
+                assert o["tokens"][b, pos] == -5
