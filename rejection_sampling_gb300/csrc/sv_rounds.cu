@@ -34,6 +34,8 @@ namespace {
 
 constexpr int kRWarps = 8;
 constexpr int kRThreads = 32 * kRWarps;
+constexpr int kLWarps = 4;  // sequences (warps) per CTA of the lane-per-position kernel
+constexpr int kLThreads = 32 * kLWarps;
 constexpr int kDraftCache = 1024;  // window positions whose draft statistics are kept
 constexpr int kLaneMaxV = 512;     // vocabularies a lane reduces alone
 
@@ -310,12 +312,12 @@ __device__ __forceinline__ Stats row_stats_lane_staged(const unsigned char* row,
 // rows' statistics alone (the draft row's once, kept in registers for the
 // first group); a ballot gives the first position that is not accepted, so a
 // round needs no block barrier; the whole warp then draws.
-__global__ void __launch_bounds__(kRThreads) rounds_lane_kernel(const __grid_constant__ RoundsParams P) {
-  __shared__ float s_rowbuf[kRWarps * 32 * 33];
+__global__ void __launch_bounds__(kLThreads) rounds_lane_kernel(const __grid_constant__ RoundsParams P) {
+  __shared__ float s_rowbuf[kLWarps * 32 * 33];
   const int lane = threadIdx.x & 31;
   float* const rslot = s_rowbuf + (threadIdx.x >> 5) * 32 * 33 + lane * 33;
   const bool staged = !P.bf16 && P.V <= 32;  // fp32 rows short enough to stage
-  const int b = blockIdx.x * kRWarps + (threadIdx.x >> 5);
+  const int b = blockIdx.x * kLWarps + (threadIdx.x >> 5);
   if (b >= P.B) return;  // whole warps only: nothing below synchronises the block
   const int R = P.R, D = P.D, V = P.V;
   const size_t es = P.bf16 ? 2 : 4;
@@ -420,7 +422,7 @@ __global__ void __launch_bounds__(kRThreads) rounds_lane_kernel(const __grid_con
 
 cudaError_t launch_rounds(const RoundsParams& p, cudaStream_t s) {
   if (p.V <= kLaneMaxV) {  // a lane per window position, a warp per sequence
-    rounds_lane_kernel<<<(p.B + kRWarps - 1) / kRWarps, kRThreads, 0, s>>>(p);
+    rounds_lane_kernel<<<(p.B + kLWarps - 1) / kLWarps, kLThreads, 0, s>>>(p);
   } else {  // a warp per window position, a CTA per sequence
     rounds_kernel<<<p.B, kRThreads, 0, s>>>(p);
   }
