@@ -38,3 +38,34 @@ def test_named_workload_shapes_and_determinism():
 def test_spikes_present():
     d = wl.dense_inputs(1, 2, 5000, dtype="f32", seed=1, spikes=8, spike_height=12.0)
     assert ((d["target"][0] > 10).sum(-1) >= 8).all()
+
+
+def test_next_row_generators():
+    # greedy: drafts are the argmax of the noisy target, so ids are in range
+    g = wl.make("greedy_b64_g7_v128256", B=3)
+    assert g["target"].shape == (3, 8, 128256) and g["draft_ids"].shape == (3, 7)
+    assert (g["draft_ids"] >= 0).all() and (g["draft_ids"] < 128256).all()
+    # commit: one spike per position, a 0/1 mask, tau in (0, 1)
+    c = wl.commit_inputs(5, 4, 3000, dtype="f32", seed=2)
+    assert c["logits"].shape == (5, 4, 3000) and set(np.unique(c["masked"])) <= {0, 1}
+    assert 0 < c["tau"] < 1
+    assert ((c["logits"] > 9).sum(-1) >= 1).all()
+    # support: the headline's target and draft rows stacked
+    s = wl.make("support_b64_g7_v128256", seed=0, B=2)
+    assert s["logits"].shape == (2 * 8 + 2 * 7, 128256) and s["K"] == 50
+    # rounds: shapes, ranges and determinism
+    r1 = wl.rounds_inputs(6, 3, 20, 9, dtype="f32", seed=4, wmax=7)
+    r2 = wl.rounds_inputs(6, 3, 20, 9, dtype="f32", seed=4, wmax=7)
+    assert r1["target"].shape == (6, 3, 20, 9) and r1["draft"].shape == (6, 20, 9)
+    assert r1["draft_tokens"].shape == (6, 3, 20) and r1["u_accept"].shape == (6, 3, 20)
+    assert r1["u_sample"].shape == (6, 3)
+    assert all(sorted(o) == list(range(20)) for o in r1["order"].tolist())
+    assert (r1["revealed"] >= 0).all() and (r1["revealed"] < 20).all()
+    assert (r1["window"] >= 1).all() and (r1["window"] <= 7).all()
+    assert (r1["draft_tokens"] >= 0).all() and (r1["draft_tokens"] < 9).all()
+    for k in ("target", "draft", "order", "revealed", "window", "draft_tokens", "u_accept", "u_sample"):
+        np.testing.assert_array_equal(r1[k], r2[k])
+    # the per-round draft tokens are fresh draws, not one draw repeated
+    assert (r1["draft_tokens"][:, 0] != r1["draft_tokens"][:, 1]).any()
+    t8 = wl.make("rounds_b4096_r4_d256_v27", seed=0, B=4)
+    assert t8["target"].shape == (4, 4, 256, 27) and t8["dtau"] == 0.05 and "window" not in t8
