@@ -46,6 +46,7 @@ NOMINAL_HBM_GBS = 8000.0
 KERNEL_SOURCES = ("rejection_sampling_gb300/csrc/sv_dense.cu",
                   "rejection_sampling_gb300/csrc/sv_common.cuh",
                   "rejection_sampling_gb300/csrc/sv_internal.h")
+PATH_ENV = "SPEC_VERIFY_DENSE_KERNELS"  # split | fused: force one large-vocabulary dense path
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "dense_b64_g7_v128256_ncu.txt")
 
 
@@ -85,6 +86,13 @@ def measured_peak():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def bench_config(B, G, V, ws):
+    """The workload description both arms print (identical dicts)."""
+    return {"workload": WORKLOAD, "B": B, "gamma": G, "V": V, "logits": "bf16",
+            "global_batch_rows": B * ws, "parallelism": f"rows sharded over {ws} GPU(s)",
+            "l2": "inputs larger than L2: two resident copies (2 x 246 MB) alternated"}
 
 
 def dist_env():
@@ -214,10 +222,22 @@ def variant_lines(dev, stream):
     import rejection_sampling_gb300 as rs
     from rejection_sampling_gb300 import workloads as wl
     out = {}
-    for name in ("dense_v32_g4", "dense_v151936_g15", "sparse_b256_g15_k64", "anyorder_b4096_w32_v33",
-                 "greedy_b64_g7_v128256", "commit_b64_w4_v151936", "support_b64_g7_v128256",
-                 "rounds_b4096_r4_d256_v27"):
-        d = wl.make(name, seed=0)
+    # (line name, workload, forced dense path or None)
+    runs = [("dense_v32_g4", "dense_v32_g4", None), ("dense_v151936_g15", "dense_v151936_g15", None),
+            ("dense_v151936_g15_two_kernel", "dense_v151936_g15", "split"),
+            ("dense_b64_g7_v128256_single_pass", "dense_b64_g7_v128256", "fused"),
+            ("sparse_b256_g15_k64", "sparse_b256_g15_k64", None),
+            ("anyorder_b4096_w32_v33", "anyorder_b4096_w32_v33", None),
+            ("greedy_b64_g7_v128256", "greedy_b64_g7_v128256", None),
+            ("commit_b64_w4_v151936", "commit_b64_w4_v151936", None),
+            ("support_b64_g7_v128256", "support_b64_g7_v128256", None),
+            ("rounds_b4096_r4_d256_v27", "rounds_b4096_r4_d256_v27", None)]
+    for name, wname, forced in runs:
+        d = wl.make(wname, seed=0)
+        if forced:
+            os.environ[PATH_ENV] = forced
+        else:
+            os.environ.pop(PATH_ENV, None)
         copies = 8  # rotate over copies so the inputs exceed L2 where they are small
         calls = []
         if d["kind"] == "dense":
@@ -225,6 +245,7 @@ def variant_lines(dev, stream):
             es = 2 if d["dtype"] == "bf16" else 4
             nbytes = dense_bytes(B, G, V, es)
             positions = B * G
+            copies = max(2, min(64, -(-300_000_000 // nbytes)))  # rotating copies > 2 x L2
             base = [to_dev(d[k], dev) for k in ("target", "draft", "draft_ids", "u_accept", "u_sample")]
             for c in range(copies):
                 args = [t.clone() for t in base]
@@ -292,6 +313,7 @@ def variant_lines(dev, stream):
             B, G, k = d["B"], d["gamma"], d["kt"]
             nbytes = B * ((G + 1) * k + G * k) * 8 + B * G * 8 + B * 4
             positions = B * G
+            copies = max(2, min(64, -(-300_000_000 // nbytes)))  # rotating copies > 2 x L2
             base = [to_dev(d[x], dev) for x in ("tgt_ids", "tgt_probs", "drf_ids", "drf_probs",
                                                 "draft_tokens", "u_accept", "u_sample")]
             for c in range(copies):
@@ -317,10 +339,13 @@ def variant_lines(dev, stream):
                      "positions_per_s": positions / (ms * 1e-3),
                      "GBps": nbytes / (ms * 1e-3) / 1e9,
                      "bytes_per_call": nbytes}
-        if d["kind"] in ("greedy", "commit", "support"):  # streaming passes over logits: HBM roofline
+        if d["kind"] in ("greedy", "commit", "support", "dense", "anyorder"):  # reads every logit once
             peak, _ = measured_peak()
             out[name]["frac_of_measured_hbm"] = out[name]["GBps"] / peak
+        if forced:
+            out[name]["dense_path"] = forced
         del calls
+    os.environ.pop(PATH_ENV, None)
     torch.cuda.synchronize()
     return out
 
@@ -479,10 +504,7 @@ def run_ours(args):
             "warmup": args.warmup, "ms_per_step": max_elapsed * 1e3 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded; bf16 logits, fp32 arithmetic)",
-            "config": {"workload": WORKLOAD, "B": B, "gamma": G, "V": V, "logits": "bf16",
-                       "global_batch_rows": B * ws, "parallelism": f"rows sharded over {ws} GPU(s)",
-                       "l2": "inputs larger than L2: two resident copies (2 x 246 MB) alternated",
-                       "preheat_s": args.preheat_s},
+            "config": bench_config(B, G, V, ws),
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_kind": peak_kind,
                          "frac_of_nominal_8TBps": achieved / NOMINAL_HBM_GBS,
@@ -543,8 +565,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded)", "config": {"workload": WORKLOAD, "B": B, "gamma": G,
-                                                 "V": d["V"], "logits": "bf16"},
+        "data": "synthetic (seeded)", "config": bench_config(B, G, d["V"], ws),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

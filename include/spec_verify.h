@@ -45,13 +45,15 @@
  *     contains NaN or +inf or is entirely -inf) do not stop the call: the
  *     offending row gets n_accepted = -1 and out_tokens = -1, and a bit is
  *     set in the workspace status word that spec_verify_check() reports.
- *   - Waits between thread blocks are only the hardware's: the dense call's
- *     second kernel is a programmatic dependent of the first
- *     (griddepcontrol.wait) and its CTAs meet at cluster barriers; the first
- *     kernel is a programmatic dependent of whatever precedes it on the
- *     stream and reads nothing before that grid has completed.  No kernel
- *     spins on memory written by another block.  (SV_ERR_TIMEOUT is kept for
- *     ABI stability; this version never reports it.)
+ *   - Waits between thread blocks are only the hardware's: the dense
+ *     kernels are programmatic dependents (griddepcontrol.wait) of whatever
+ *     precedes them on the stream and read nothing before that grid has
+ *     completed; the CTAs of a thread-block cluster meet at cluster
+ *     barriers.  No kernel spins on memory written by another block.  The
+ *     single-pass dense kernel waits on its own bulk copies into shared
+ *     memory, for about one second at most: a copy that has not landed by
+ *     then gives its row n_accepted = -1 and sets the timeout bit, which
+ *     spec_verify_check reports as SV_ERR_TIMEOUT.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -73,7 +75,7 @@ typedef enum sv_status {
   SV_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no GPU) */
   SV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
   SV_ERR_DEVICE_INPUT = 4, /* spec_verify_check: some row had invalid inputs   */
-  SV_ERR_TIMEOUT = 5,      /* reserved: a bounded device wait ran out        */
+  SV_ERR_TIMEOUT = 5,      /* spec_verify_check: a bounded copy wait ran out */
   SV_ERR_SCRATCH_LIMIT = 6 /* spec_verify_dense_static: sizes need more scratch
                               than SV_STATIC_SCRATCH_BYTES; nothing launched  */
 } sv_status;
@@ -124,9 +126,18 @@ sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream
  * Softmax, gather, ratio test, first-reject scan and the inverse-CDF draw run
  * in fp32, with partial sums combined and prefixed in float-float (pairs of
  * fp32 carrying ~48 significant bits); bf16 inputs are widened exactly.
- * Large vocabularies take two kernels: the first reads every logit once
- * (statistics, gather, accept tests, first rejection), the second reads the
- * two rows of each row's stop position again (residual masses and the draw).
+ * Paths (chosen per call, the same results up to rounding):
+ *   - (gamma + 1) * V small enough for one warp: a warp per row;
+ *   - rows of a 16-byte multiple with 16-byte aligned bases, and a grid that
+ *     is resident all at once: one pass, a thread-block cluster per (row,
+ *     position) holding both rows in shared memory, the draw taken from
+ *     shared memory (a rejected or bonus position draws speculatively; the
+ *     row's first rejection keeps its draw);
+ *   - otherwise two kernels: the first reads every logit once (statistics,
+ *     gather), the second takes the decisions and reads the two rows of each
+ *     row's stop position again (residual masses and the draw).
+ *   The environment variable SPEC_VERIFY_DENSE_KERNELS=split or =fused
+ *   forces the two-kernel or the single-pass path (measurement switch).
  */
 int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dtype dtype,
                       const int32_t* draft_ids, const float* u_accept, const float* u_sample,
@@ -296,9 +307,10 @@ int spec_support_topk(const void* logits, sv_dtype dtype, int N, int V, float te
 
 /*
  * spec_verify_check -- synchronise `stream`, read and clear the workspace
- * status word.  Returns SV_OK, SV_ERR_DEVICE_INPUT (some row of an earlier
- * call had invalid inputs; those rows carry n_accepted = -1),
- * or SV_ERR_CUDA.
+ * status word.  Returns SV_OK, SV_ERR_TIMEOUT (a bulk copy of the single-pass
+ * dense kernel did not land within its bounded wait; that row carries
+ * n_accepted = -1), SV_ERR_DEVICE_INPUT (some row of an earlier call had
+ * invalid inputs; those rows carry n_accepted = -1), or SV_ERR_CUDA.
  */
 int spec_verify_check(void* workspace, size_t ws_bytes, sv_stream_t stream);
 
@@ -322,22 +334,26 @@ const char* spec_verify_status_string(int status);
  *
  * The scratch: a file-scope device array of SV_STATIC_SCRATCH_BYTES (4 MiB),
  * which every GPU that loads the library holds until the process exits.  A
- * call needs spec_verify_workspace_size(B, gamma, V) bytes of it (for example
- * 0.33 MiB at B = 64, gamma = 7, V = 128256; 2.75 MiB at B = 256, gamma = 15,
- * V = 151936); larger sizes return SV_ERR_SCRATCH_LIMIT and launch nothing.
+ * call uses what the path it takes needs (see spec_verify_dense): 256 bytes
+ * on the warp-per-row path; 256 + 2 x 4 B + 32 B (gamma + 1) bytes (each
+ * part rounded up to 256 bytes) on the single-pass path (17 KB at B = 64,
+ * gamma = 7); on the two-kernel path 32 bytes per 2 KB piece of every row
+ * and position plus small terms (0.33 MiB at B = 64, gamma = 7, V = 128256
+ * bf16).  Larger needs return SV_ERR_SCRATCH_LIMIT and launch nothing: sizes
+ * that exceed the array on every path are refused on the host before any
+ * CUDA call, the rest once the path is known.
  *   - Set-up: the first call on each device looks up the array's device
  *     address (cudaGetSymbolAddress, with that device current) and keeps it.
  *     That look-up may load the library's device code, so make the first
  *     call on each device before any stream capture.
- *   - Every call shares the array.  A call clears the part it uses (and sets
- *     n_accepted to -1) on `stream` before its kernels run, so state left by
- *     an earlier call never leaks in; calls whose work may overlap on the GPU
- *     (other streams, other host threads) race on the array and must be
- *     ordered by the caller.
+ *   - Every call shares the array.  A call clears the part it uses on
+ *     `stream` before its kernels run, so state left by an earlier call never
+ *     leaks in; calls whose work may overlap on the GPU (other streams, other
+ *     host threads) race on the array and must be ordered by the caller.
  *   - Errors: host-side argument errors as spec_verify_dense (nothing
- *     launched).  There is no status word to query: rows with invalid inputs,
- *     and rows a call left unfinished because a bounded wait ran out, carry
- *     n_accepted = -1.
+ *     launched).  There is no status word to query: rows with invalid inputs
+ *     (and, on the single-pass path, rows whose bulk copy did not land
+ *     within the bounded wait) carry n_accepted = -1.
  */
 #define SV_STATIC_SCRATCH_BYTES (4u << 20)
 int spec_verify_dense_static(const void* target_logits, const void* draft_logits, sv_dtype dtype,

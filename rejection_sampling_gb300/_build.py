@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OBJ_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libspec_verify.so")
-SOURCES = ["sv_api.cu", "sv_dense.cu", "sv_greedy.cu", "sv_small.cu", "sv_sparse.cu", "sv_static.cu",
+SOURCES = ["sv_api.cu", "sv_dense.cu", "sv_fused.cu", "sv_greedy.cu", "sv_small.cu", "sv_sparse.cu", "sv_static.cu",
            "sv_rounds.cu", "sv_support.cu"]
 HEADERS = [os.path.join(CSRC, h) for h in ("sv_common.cuh", "sv_internal.h")] + [
     os.path.join(ROOT, "include", "spec_verify.h")]

@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <math.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/spec_verify.h"
@@ -26,7 +27,52 @@ size_t dense_ws_bytes(long long B, int G, int V, int es) {
 
 sv_status launch_status(cudaError_t e) { return e == cudaSuccess ? SV_OK : SV_ERR_CUDA; }
 
+// Which path takes a large-vocabulary dense call.  By default the
+// single-pass cluster kernel when its whole grid is resident at once, else
+// the two-kernel path (statistics kernel + row kernel).  The environment
+// variable SPEC_VERIFY_DENSE_KERNELS=split or =fused forces one of them (the
+// fused kernel still needs 16-byte rows): a measurement and diagnosis switch,
+// read on every call.
+enum DensePath { kPathAuto = 0, kPathSplit = 1, kPathFused = 2 };
+int dense_path_env() {
+  const char* v = getenv("SPEC_VERIFY_DENSE_KERNELS");
+  if (!v) return kPathAuto;
+  if (strcmp(v, "split") == 0) return kPathSplit;
+  if (strcmp(v, "fused") == 0) return kPathFused;
+  return kPathAuto;
+}
+
+// cluster size (> 0) if the fused kernel takes this call, 0 if the two-kernel
+// path does, -1 on a CUDA error
+int dense_fused_choice(const void* tl, const void* dl, int B, int gamma, int V, int es, int* L) {
+  const int path = dense_path_env();
+  if (path == kPathSplit) return 0;
+  if (!(((size_t)V * es) % 16 == 0 && aligned_to(tl, 16) && (gamma == 0 || aligned_to(dl, 16))))
+    return 0;
+  return sv::fused_plan(B, gamma, V, es, path != kPathFused, L);
+}
+
+
 }  // namespace
+
+namespace sv {
+// Workspace bytes that spec_verify_dense touches for these arguments (the
+// path it will take): 0 on a CUDA error.
+size_t dense_workspace_need(const void* target_logits, const void* draft_logits, int es, int B,
+                            int gamma, int V) {
+  if (small_fits(gamma + 1, V)) return sizeof(WsHeader);
+  int L = 0;
+  const int C = dense_fused_choice(target_logits, draft_logits, B, gamma, V, es, &L);
+  if (C < 0) return 0;
+  if (C > 0) return fused_layout(B, gamma).total;
+  return dense_layout(B, gamma, dense_geom(V, es)).total;
+}
+size_t dense_workspace_floor(int B, int gamma, int V) {
+  if (small_fits(gamma + 1, V)) return sizeof(WsHeader);
+  // the single-pass layout is the smaller of the two large-vocabulary ones
+  return fused_layout(B, gamma).total;
+}
+}  // namespace sv
 
 extern "C" {
 
@@ -92,6 +138,41 @@ int spec_verify_dense(const void* target_logits, const void* draft_logits, sv_dt
              ((size_t)gamma * V * 4) % 16 == 0 && aligned_to(target_logits, 16) &&
              (gamma == 0 || aligned_to(draft_logits, 16));
     return launch_status(sv::launch_small(p, s));
+  }
+
+  {
+    int Ls = 0;
+    const int C = dense_fused_choice(target_logits, draft_logits, B, gamma, V, es, &Ls);
+    if (C < 0) return SV_ERR_CUDA;
+    if (C > 0) {  // one pass: a thread-block cluster per (row, position)
+      const sv::FusedLayout FL = sv::fused_layout(B, gamma);
+      if (ws_bytes < FL.total) return SV_ERR_INVALID_ARG;
+      unsigned char* ws = static_cast<unsigned char*>(workspace);
+      sv::FusedParams f;
+      memset(&f, 0, sizeof f);
+      f.lt = static_cast<const unsigned char*>(target_logits);
+      f.ld = static_cast<const unsigned char*>(draft_logits);
+      f.x = draft_ids;
+      f.u_acc = u_accept;
+      f.u_s = u_sample;
+      f.n_out = n_accepted;
+      f.tok_out = out_tokens;
+      f.acc_out = accept_prob_out;
+      f.status = &hdr->status;
+      f.cnt = reinterpret_cast<uint32_t*>(ws + FL.cnt);
+      f.rej = reinterpret_cast<uint32_t*>(ws + FL.rej);
+      f.rec = reinterpret_cast<sv::UnitRec*>(ws + FL.rec);
+      f.B = B;
+      f.G = gamma;
+      f.V = V;
+      f.bf16 = (dtype == SV_BF16);
+      f.L = Ls;
+      f.keep_stop = residual_out != nullptr;
+      if (sv::launch_dense_fused(f, C, s) != cudaSuccess) return SV_ERR_CUDA;
+      if (residual_out && sv::launch_dense_fused_resid_out(f, residual_out, s) != cudaSuccess)
+        return SV_ERR_CUDA;
+      return SV_OK;
+    }
   }
 
   const sv::DenseGeom g = sv::dense_geom(V, es);

@@ -106,6 +106,74 @@ struct DenseParams {
 };
 
 // ---------------------------------------------------------------------------
+// dense, single pass: one thread-block cluster per (row, position) unit
+// ---------------------------------------------------------------------------
+// Outcome of one unit, written by the CTA that finished it (32 bytes).
+struct UnitRec {
+  uint32_t flags;      // kRec* bits
+  int32_t token;       // the draw at this position (kRecDrawn)
+  float ct, cd;        // log2e * max of the target / draft row
+  float invSt, invSd;  // 1 / sum 2^(v log2e - c) of the target / draft row
+  float T_hi, T_lo;    // total mass of the distribution the draw walked
+};
+static_assert(sizeof(UnitRec) == 32, "unit record is 32 bytes");
+enum : uint32_t {
+  kRecAccept = 1u,   // the draft token was accepted
+  kRecErr = 2u,      // input error in this unit
+  kRecPDraw = 4u,    // the draw used p (bonus, or a zero residual)
+  kRecDrawn = 8u,    // token holds a draw
+  kRecTimeout = 16u  // a bulk copy did not land within the bounded wait
+};
+
+struct FusedLayout {  // byte offsets into the workspace
+  size_t cnt, rej, rec, total;
+};
+inline FusedLayout fused_layout(long long B, int G) {
+  FusedLayout L;
+  size_t o = sizeof(WsHeader);
+  L.cnt = o;  // per row: units that have finished
+  o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
+  L.rej = o;  // per row: G + 1 - j of the earliest rejection seen so far (0: none)
+  o = align_up(o + sizeof(uint32_t) * (size_t)B, 256);
+  L.rec = o;  // [B, G + 1] unit records
+  o = align_up(o + sizeof(UnitRec) * (size_t)B * (size_t)(G + 1), 256);
+  L.total = o;
+  return L;
+}
+
+struct FusedParams {
+  const unsigned char* lt;  // [B, G+1, V]
+  const unsigned char* ld;  // [B, G, V]
+  const int32_t* x;         // [B, G]
+  const float* u_acc;       // [B, G]
+  const float* u_s;         // [B]
+  int32_t* n_out;           // [B]
+  int32_t* tok_out;         // [B, G+1]
+  float* acc_out;           // [B, G] or null
+  uint32_t* status;         // workspace status word
+  uint32_t* cnt;            // [B]
+  uint32_t* rej;            // [B]
+  UnitRec* rec;             // [B, G+1]
+  int B, G, V;
+  int bf16;
+  int L;          // elements of a row per cluster rank (a multiple of 16 / element size)
+  int keep_stop;  // residual_out follows: the stop record of each row is kept for it
+};
+
+// Cluster size of the single-pass kernel for these sizes, with the slice
+// length in *L_out; 0: the call goes to the two-kernel path (rows not a
+// multiple of 16 bytes, slices too long, or -- with single_wave -- a grid
+// that is not resident all at once); -1: CUDA error.
+int fused_plan(long long B, int G, int V, int es, bool single_wave, int* L_out);
+cudaError_t launch_dense_fused(const FusedParams& p, int C, cudaStream_t s);
+cudaError_t launch_dense_fused_resid_out(const FusedParams& p, float* resid_out, cudaStream_t s);
+// workspace bytes the dense call touches on the path it takes (0: CUDA error)
+size_t dense_workspace_need(const void* target_logits, const void* draft_logits, int es, int B,
+                            int gamma, int V);
+// the least of those over every path these sizes can take (host only, no CUDA call)
+size_t dense_workspace_floor(int B, int gamma, int V);
+
+// ---------------------------------------------------------------------------
 // small-vocabulary warp-per-row kernel (dense and any-order)
 // ---------------------------------------------------------------------------
 struct SmallParams {

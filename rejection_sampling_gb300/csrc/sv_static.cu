@@ -20,13 +20,18 @@
 // Every call shares the one array: it clears the part it uses on the stream
 // before the kernels run (so nothing a previous call left behind, finished
 // or not, can leak in), and two calls whose work overlaps on the GPU -- on
-// different streams, or from different host threads -- race on it.
+// different streams, or from different host threads -- race on it.  The part
+// a call uses is what the path it takes needs: the header alone for short
+// vocabularies (the warp-per-row kernel), the per-row words and per-position
+// records of the single-pass kernel, or the piece records of the two-kernel
+// path; only the last depends on V.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include <mutex>
 
 #include "../../include/spec_verify.h"
+#include "sv_internal.h"
 
 namespace {
 
@@ -64,8 +69,10 @@ extern "C" int spec_verify_dense_static(const void* target_logits, const void* d
   if (B < 0 || gamma < 0 || gamma > SV_MAX_GAMMA || V < 1 || V > SV_MAX_VOCAB) return SV_ERR_INVALID_ARG;
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_INVALID_ARG;
   if (B == 0) return SV_OK;
-  const size_t need = spec_verify_workspace_size(B, gamma, V);
-  if (need == 0 || need > (size_t)SV_STATIC_SCRATCH_BYTES) return SV_ERR_SCRATCH_LIMIT;
+  // sizes whose workspace exceeds the array on every path are refused first,
+  // on the host alone (no CUDA call)
+  if (sv::dense_workspace_floor(B, gamma, V) > (size_t)SV_STATIC_SCRATCH_BYTES)
+    return SV_ERR_SCRATCH_LIMIT;
   if (!target_logits || !u_sample || !n_accepted || !out_tokens) return SV_ERR_INVALID_ARG;
   if (gamma > 0 && (!draft_logits || !draft_ids || !u_accept)) return SV_ERR_INVALID_ARG;
   const size_t es = (dtype == SV_BF16) ? 2 : 4;
@@ -77,15 +84,18 @@ extern "C" int spec_verify_dense_static(const void* target_logits, const void* d
       (accept_prob_out && !aligned(accept_prob_out, 4)))
     return SV_ERR_INVALID_ARG;
 
+  // the workspace bytes of the path this call takes (the same choice
+  // spec_verify_dense makes from the same arguments)
+  const size_t need = sv::dense_workspace_need(target_logits, draft_logits, (int)es, B, gamma, V);
+  if (need == 0) return SV_ERR_CUDA;
+  if (need > (size_t)SV_STATIC_SCRATCH_BYTES) return SV_ERR_SCRATCH_LIMIT;
+
   void* scratch = nullptr;
   const int rc = scratch_for_current_device(&scratch);
   if (rc != SV_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
-  // the counters, queues and status word must start at zero; rows that a call
-  // does not finish (only after a bounded wait ran out) read n_accepted = -1
+  // the counters, records and status word must start at zero
   if (cudaMemsetAsync(scratch, 0, need, s) != cudaSuccess) return SV_ERR_CUDA;
-  if (cudaMemsetAsync(n_accepted, 0xFF, (size_t)B * sizeof(int32_t), s) != cudaSuccess)
-    return SV_ERR_CUDA;
   return spec_verify_dense(target_logits, draft_logits, dtype, draft_ids, u_accept, u_sample, B,
                            gamma, V, n_accepted, out_tokens, residual_out, accept_prob_out,
                            scratch, need, stream);

@@ -103,3 +103,53 @@ def check_dense_residual(gpu_res, gpu_n, ora, target, draft, G):
         atol = PROB_RTOL * (p + q) / T + 1e-12
         err = np.abs(gpu_res[b].astype(np.float64) - w)
         assert (err <= atol + PROB_RTOL * np.abs(w)).all(), (b, err.max())
+
+
+def check_anyorder_residual(gpu_res, gpu_n, ora, target, draft, order, W):
+    """Any-order residual_out within 1e-5 of the operands p + q (divided by T)
+    at the stop position sigma(n), on rows where the GPU and the oracle
+    stopped at the same window index; all-zero on rows that accepted the
+    whole window (no bonus) and on input-error rows."""
+    lt, ld = widen(target), widen(draft)
+    for b in range(len(ora["n_accepted"])):
+        n = int(ora["n_accepted"][b])
+        if n != int(gpu_n[b]):
+            continue
+        if n < 0 or n == W:
+            assert (gpu_res[b] == 0).all(), b
+            continue
+        s = int(order[b, n])
+        w = ora["residual"][b]
+        T = ora["resid_mass"][b]
+        p = softmax64(lt[b, s])
+        q = softmax64(ld[b, s]) if not (ora["flags"][b] & 4) else np.zeros_like(p)
+        atol = PROB_RTOL * (p + q) / T + 1e-12
+        err = np.abs(gpu_res[b].astype(np.float64) - w)
+        assert (err <= atol + PROB_RTOL * np.abs(w)).all(), (b, err.max())
+
+
+def check_anyorder_flagged(gpu_n, gpu_tok, ora, draft_tokens, order, u_s, init):
+    """Rows the oracle flags must still hold a valid any-order outcome: the
+    accepted prefix (in sigma order) keeps the draft tokens, the token at
+    sigma(n) lies on the oracle's CDF within the tie band, the rest of the
+    window is -1, and positions outside the window are untouched.  Input-error
+    rows must agree exactly (n = -1, the window -1)."""
+    fl = ora["flags"]
+    B, W = order.shape
+    for b in np.nonzero(fl != 0)[0]:
+        sig = order[b]
+        outside = np.ones(gpu_tok.shape[1], bool)
+        outside[sig] = False
+        assert (gpu_tok[b, outside] == init[b, outside]).all(), b
+        n = int(gpu_n[b])
+        if fl[b] & 8:
+            assert n == -1 and (gpu_tok[b, sig] == -1).all(), b
+            continue
+        assert 0 <= n <= W, (b, n)
+        assert (gpu_tok[b, sig[:n]] == draft_tokens[b, sig[:n]]).all(), b
+        assert (gpu_tok[b, sig[n + 1:]] == -1).all(), b
+        if n < W:
+            y = int(gpu_tok[b, sig[n]])
+            assert y >= 0, b
+            if n == int(ora["n_accepted"][b]) and not (fl[b] & 4):
+                assert cdf_consistent(ora["residual"][b], float(u_s[b]), y), (b, y)
