@@ -574,9 +574,9 @@ def run_reference(args):
 
 def run_calls_only(args):
     """Profiling driver: args.calls_only untimed calls of one workload (the
-    headline by default; ``--workload NAME`` for the greedy, commit, support
-    and rounds paths), no output beyond one status line (ncu's launch filters pick the
-    kernels out)."""
+    headline by default; ``--workload NAME`` for any other named workload), no
+    output beyond one status line (ncu's launch filters pick the kernels
+    out)."""
     import torch
     import rejection_sampling_gb300 as rs
     from rejection_sampling_gb300 import workloads as wl
@@ -604,9 +604,16 @@ def run_calls_only(args):
         t = [to_dev(x, dev) for x in (d["target"], d["draft"], d["order"], d["revealed"], window,
                                       d["draft_tokens"], d["u_accept"], d["u_sample"])]
         fn = rs.spec_verify_anyorder_rounds
+    elif d["kind"] == "sparse":
+        t = [to_dev(d[x], dev) for x in ("tgt_ids", "tgt_probs", "drf_ids", "drf_probs",
+                                         "draft_tokens", "u_accept", "u_sample")] + [d["V"]]
+        fn = rs.spec_verify_sparse
+    elif d["kind"] == "anyorder":
+        t = [to_dev(d[x], dev) for x in ("target", "draft", "order", "draft_tokens", "u_accept",
+                                         "u_sample")]
+        fn = rs.spec_verify_anyorder
     else:
-        raise SystemExit(f"--calls-only drives dense, greedy, commit, support and rounds workloads, "
-                         f"not {name}")
+        raise SystemExit(f"--calls-only cannot drive workload {name}")
     for _ in range(args.calls_only):
         fn(*t)
     torch.cuda.synchronize()

@@ -139,6 +139,33 @@ __device__ __forceinline__ ff warp_sum_ff(ff v) {
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// partial softmax sums with integer reference points.  A partial sum is
+// S = sum 2^(v log2e - c) with c = ceil(log2e * max v): every rescale between
+// partials is then an exact power of two, formed on the integer pipe (no
+// MUFU, no rounding).
+// ---------------------------------------------------------------------------
+// 2^d for an integer-valued d <= 0 (0 below the normal range, and for NaN)
+__device__ __forceinline__ float pow2i(float d) {
+  return d > -127.f ? __int_as_float(((int)d + 127) << 23) : 0.f;
+}
+// the reference point of a partial whose largest element is m
+__device__ __forceinline__ float ref_point(float m) {
+  return (m == -INFINITY) ? -INFINITY : ceilf(m * kLog2e);
+}
+// 2^(c - C): a partial with reference c moved to reference C >= c (0 for an
+// all -inf partial)
+__device__ __forceinline__ float scale_exact(float c, float C) {
+  return (c == -INFINITY) ? 0.f : pow2i(c - C);
+}
+// order-preserving map of fp32 onto int32, so one redux.sync finds a warp's
+// largest float
+__device__ __forceinline__ int f2ord(float f) {
+  const int i = __float_as_int(f);
+  return i >= 0 ? i : i ^ 0x7FFFFFFF;
+}
+__device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF); }
+
 // exclusive prefix over lanes
 __device__ __forceinline__ ff warp_exclusive_scan_ff(ff v, int lane) {
   ff x = v;
@@ -148,6 +175,24 @@ __device__ __forceinline__ ff warp_exclusive_scan_ff(ff v, int lane) {
     if (lane >= o) x = ff_add(x, y);
   }
   return ff_sub(x, v);
+}
+
+// warp-wide combination of per-lane (C, S) partials of two rows: the
+// reference points by redux.sync, the exactly rescaled sums by one shuffle
+// tree (float-float); every lane ends with the warp's totals
+__device__ __forceinline__ void warp_combine_pair(float& Ct, ff& St, float& Cd, ff& Sd) {
+  const float Cwt = ord2f(__reduce_max_sync(0xffffffffu, f2ord(Ct)));
+  const float Cwd = ord2f(__reduce_max_sync(0xffffffffu, f2ord(Cd)));
+  St = ff_mul_f(St, scale_exact(Ct, Cwt));
+  Sd = ff_mul_f(Sd, scale_exact(Cd, Cwd));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const ff a = ff_shfl_xor(St, o), b = ff_shfl_xor(Sd, o);
+    St = ff_add(St, a);
+    Sd = ff_add(Sd, b);
+  }
+  Ct = Cwt;
+  Cd = Cwd;
 }
 
 }  // namespace sv

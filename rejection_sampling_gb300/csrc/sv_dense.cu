@@ -157,16 +157,18 @@ __device__ __forceinline__ void load_piece(const unsigned char* base, int ne, in
   }
 }
 
-// (c, S) of a piece: c = log2e * max, S = sum 2^(v log2e - c); an all -inf
-// piece gives c = -inf, S = 0 (its exponentials use c = 0, so a NaN still
-// poisons S)
-__device__ __forceinline__ void piece_stats(const uint4 (&r)[4], int bf16, float& c_out,
-                                            float& s_out) {
+// Fold this lane's 32 elements of a piece (its four 16-byte vectors) into its
+// running (C, S): the integer reference point C = ceil(log2e * max) grows
+// when the piece holds a larger element (the sum is then rescaled exactly),
+// then S += sum 2^(v log2e - C).  A NaN element makes S NaN, -inf elements
+// add 0, and an all -inf lane keeps C = -inf, S = 0.  No cross-lane work:
+// the lanes of a warp are combined once, when its range leaves the segment.
+__device__ __forceinline__ void lane_fold(const uint4 (&r)[4], int bf16, float& C, ff& S) {
   float m;
   if (bf16) {
-    uint32_t mx = kNegInf2;
+    uint32_t mx = bf16x2_max(bf16x2_max(r[0].x, r[0].y), bf16x2_max(r[0].z, r[0].w));
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+    for (int i = 1; i < 4; ++i)
       mx = bf16x2_max(mx, bf16x2_max(bf16x2_max(r[i].x, r[i].y), bf16x2_max(r[i].z, r[i].w)));
     m = fmaxf(bf16_lo(mx), bf16_hi(mx));
   } else {
@@ -176,32 +178,35 @@ __device__ __forceinline__ void piece_stats(const uint4 (&r)[4], int bf16, float
       m = fmaxf(m, fmaxf(fmaxf(__uint_as_float(r[i].x), __uint_as_float(r[i].y)),
                          fmaxf(__uint_as_float(r[i].z), __uint_as_float(r[i].w))));
   }
-  m = warp_max(m);
-  const float c = (m == -INFINITY) ? 0.f : m * kLog2e;
+  const float c = ref_point(m);
+  if (c > C) {
+    S = ff_mul_f(S, scale_exact(C, c));
+    C = c;
+  }
+  const float cc = (C == -INFINITY) ? 0.f : C;
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (bf16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -c));
-      a1 += ex2(fmaf(bf16_hi(r[i].x), kLog2e, -c));
-      a2 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -c));
-      a3 += ex2(fmaf(bf16_hi(r[i].y), kLog2e, -c));
-      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -c));
-      a1 += ex2(fmaf(bf16_hi(r[i].z), kLog2e, -c));
-      a2 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -c));
-      a3 += ex2(fmaf(bf16_hi(r[i].w), kLog2e, -c));
+      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -cc));
+      a1 += ex2(fmaf(bf16_hi(r[i].x), kLog2e, -cc));
+      a2 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -cc));
+      a3 += ex2(fmaf(bf16_hi(r[i].y), kLog2e, -cc));
+      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -cc));
+      a1 += ex2(fmaf(bf16_hi(r[i].z), kLog2e, -cc));
+      a2 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -cc));
+      a3 += ex2(fmaf(bf16_hi(r[i].w), kLog2e, -cc));
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -c));
-      a1 += ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -c));
-      a2 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -c));
-      a3 += ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -c));
+      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -cc));
+      a1 += ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -cc));
+      a2 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -cc));
+      a3 += ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -cc));
     }
   }
-  s_out = warp_sum((a0 + a1) + (a2 + a3));
-  c_out = (m == -INFINITY) ? -INFINITY : c;
+  S = ff_add_f(S, (a0 + a1) + (a2 + a3));
 }
 
 // fp32 bits of element xl (0 <= xl < ne) of the piece, on every lane
@@ -518,28 +523,35 @@ __device__ __forceinline__ void issue_item(const DenseParams& P, const Item& it,
   }
 }
 
-// Running statistics of the (row, position) segment a warp is streaming: the
-// pieces of one segment are folded together (float-float) and written as one
-// record, in the slot of the segment's first piece; the other slots of the
-// segment stay zero ("empty": St = 0 and c = 0, which no real record has).
+// Running statistics of the (row, position) segment a warp is streaming:
+// each lane folds its elements of every piece of the segment into its own
+// (C, S); when the warp's range leaves the segment the lanes are combined
+// and written as one record, in the slot of the segment's first piece; the
+// other slots of the segment stay zero ("empty": St = 0 and c = 0, which no
+// real record has).
 struct SegAcc {
   long long w0;  // record slot: the segment's first piece
   int b, j;
-  float Ct, Cd;
-  ff St, Sd;
+  int x;         // the segment's draft token (-1 at the bonus position)
+  float Ct, Cd;  // this lane's reference points
+  ff St, Sd;     // this lane's sums
   uint32_t tb, db;  // logits at the draft token, if a piece of the segment held it
 };
 
-__device__ __forceinline__ void seg_begin(SegAcc& a, const Item& it, long long w) {
+__device__ __forceinline__ void seg_begin(SegAcc& a, const Item& it, long long w,
+                                          const DenseParams& P) {
   a.w0 = w;
   a.b = it.b;
   a.j = it.j;
+  a.x = (it.j < P.G) ? __ldg(P.x + (size_t)it.b * P.G + it.j) : -1;
   a.Ct = a.Cd = -INFINITY;
   a.St = a.Sd = ff{0.f, 0.f};
   a.tb = a.db = kNoTokenBits;
 }
 
-__device__ __forceinline__ void seg_write(const DenseParams& P, const SegAcc& a, int lane) {
+// every lane (the lanes are combined first)
+__device__ __forceinline__ void seg_write(const DenseParams& P, SegAcc& a, int lane) {
+  warp_combine_pair(a.Ct, a.St, a.Cd, a.Sd);
   if (lane == 0) {
     float4* q = reinterpret_cast<float4*>(ws_at<UnitPart>(P, P.L.upart) + a.w0);
     q[0] = make_float4(a.St.hi, a.St.lo, a.Sd.hi, a.Sd.lo);
@@ -547,33 +559,18 @@ __device__ __forceinline__ void seg_write(const DenseParams& P, const SegAcc& a,
   }
 }
 
-// fold (c, s) of one piece into a running (C, S); the rescale factor is one
-// ex2.approx (relative error ~2^-22), 0 for an all -inf side
-__device__ __forceinline__ void fold(float c, float s, float& C, ff& S) {
-  if (c > C) {
-    S = ff_add(ff_mul_f(S, (C == -INFINITY) ? 0.f : ex2(C - c)), ff{s, 0.f});
-    C = c;
-  } else {
-    S = ff_add(S, two_prod(s, (c == -INFINITY) ? 0.f : ex2(c - C)));
-  }
-}
-
-// reduce piece `it` held in rt / rd into the warp's segment accumulator
+// fold piece `it`, held in rt / rd, into this lane's segment statistics; the
+// warp whose piece holds the draft token keeps the two logits there
 __device__ __forceinline__ void piece_accumulate(const DenseParams& P, const Item& it,
                                                  const uint4 (&rt)[4], const uint4 (&rd)[4],
                                                  int lane, SegAcc& a) {
   const int pe = P.g.pe;
-  const bool has_d = it.j < P.G;
-  float ct, st;
-  piece_stats(rt, P.bf16, ct, st);
-  fold(ct, st, a.Ct, a.St);
-  if (has_d) {
-    float cd, sd;
-    piece_stats(rd, P.bf16, cd, sd);
-    fold(cd, sd, a.Cd, a.Sd);
+  lane_fold(rt, P.bf16, a.Ct, a.St);
+  if (it.j < P.G) {
+    lane_fold(rd, P.bf16, a.Cd, a.Sd);
     const int ne = min(pe, P.V - it.k * pe);
-    const int xl = __ldg(P.x + (size_t)it.b * P.G + it.j) - it.k * pe;
-    if (xl >= 0 && xl < ne) {
+    const int xl = a.x - it.k * pe;
+    if (a.x >= 0 && xl >= 0 && xl < ne) {
       a.tb = piece_element(rt, xl, P.bf16, lane);
       a.db = piece_element(rd, xl, P.bf16, lane);
     }
@@ -602,11 +599,11 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
   if (!P.aligned) {  // rows not 16-byte aligned: plain loads, no ring
     Item it = item_at(lo, G, np);
     SegAcc acc;
-    seg_begin(acc, it, lo);
+    seg_begin(acc, it, lo, P);
     for (long long w = lo; w < hi; ++w, item_next(it, G, np)) {
       if (it.b != acc.b || it.j != acc.j) {
         seg_write(P, acc, lane);
-        seg_begin(acc, it, w);
+        seg_begin(acc, it, w, P);
       }
       const int ne = min(pe, P.V - it.k * pe);
       const size_t off = (size_t)it.k * kPieceBytes;
@@ -636,11 +633,11 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
   }
   int slot = 0, islot = kStages - 1;
   SegAcc acc;
-  seg_begin(acc, out, lo);
+  seg_begin(acc, out, lo, P);
   for (long long w = lo; w < hi; ++w) {
     if (out.b != acc.b || out.j != acc.j) {
       seg_write(P, acc, lane);
-      seg_begin(acc, out, w);
+      seg_begin(acc, out, w, P);
     }
     if (wi < hi) {
       issue_item(P, in, ring + islot * kStageBytes, lane);
@@ -653,13 +650,23 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
     const int ne = min(pe, P.V - out.k * pe);
     const bool has_d = out.j < G;
     uint4 rt[4], rd[4];
+    if (ne == pe) {  // a whole piece: every vector is valid
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int vi = lane + 32 * i;
-      const bool v = vi * epv < ne;
-      rt[i] = v ? *reinterpret_cast<const uint4*>(stage + 16 * vi) : make_uint4(ninf, ninf, ninf, ninf);
-      rd[i] = (v && has_d) ? *reinterpret_cast<const uint4*>(stage + kPieceBytes + 16 * vi)
-                           : make_uint4(ninf, ninf, ninf, ninf);
+      for (int i = 0; i < 4; ++i) rt[i] = *reinterpret_cast<const uint4*>(stage + 16 * (lane + 32 * i));
+      if (has_d) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rd[i] = *reinterpret_cast<const uint4*>(stage + kPieceBytes + 16 * (lane + 32 * i));
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int vi = lane + 32 * i;
+        const bool v = vi * epv < ne;
+        rt[i] = v ? *reinterpret_cast<const uint4*>(stage + 16 * vi) : make_uint4(ninf, ninf, ninf, ninf);
+        rd[i] = (v && has_d) ? *reinterpret_cast<const uint4*>(stage + kPieceBytes + 16 * vi)
+                             : make_uint4(ninf, ninf, ninf, ninf);
+      }
     }
     piece_accumulate(P, out, rt, rd, lane, acc);
     item_next(out, G, np);

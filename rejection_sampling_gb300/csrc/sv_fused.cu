@@ -134,44 +134,9 @@ __device__ __forceinline__ uint32_t ldcg_u32(const uint32_t* p) { return __ldcg(
 // ---------------------------------------------------------------------------
 // arithmetic shared by every step
 // ---------------------------------------------------------------------------
-// The reference point c of every partial sum S = sum 2^(v log2e - c) is an
-// integer, c = ceil(log2e * max): every rescale between partial sums is then
-// an exact power of two, formed on the integer pipe (no MUFU, no rounding).
-// 2^d for an integer-valued d <= 0 (0 below the normal range, and for NaN).
-__device__ __forceinline__ float pow2i(float d) {
-  return d > -127.f ? __int_as_float(((int)d + 127) << 23) : 0.f;
-}
-__device__ __forceinline__ float ref_point(float m) {
-  return (m == -INFINITY) ? -INFINITY : ceilf(m * kLog2e);
-}
-// scale 2^(c - C) of a partial with reference c into reference C >= c
-// (0 for an all -inf part)
-__device__ __forceinline__ float part_scale(float c, float C) {
-  return (c == -INFINITY) ? 0.f : pow2i(c - C);
-}
-// order-preserving map of fp32 onto int32, so that one redux.sync finds a
-// warp's largest float
-__device__ __forceinline__ int f2ord(float f) {
-  const int i = __float_as_int(f);
-  return i >= 0 ? i : i ^ 0x7FFFFFFF;
-}
-__device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF); }
-// warp-wide combination of per-lane (C, S) pairs of both rows: the maxima by
-// redux.sync, the exactly rescaled sums by one shuffle tree (float-float)
-__device__ __forceinline__ void warp_combine2(float& Ct, ff& St, float& Cd, ff& Sd) {
-  const float Cwt = ord2f(__reduce_max_sync(0xffffffffu, f2ord(Ct)));
-  const float Cwd = ord2f(__reduce_max_sync(0xffffffffu, f2ord(Cd)));
-  St = ff_mul_f(St, part_scale(Ct, Cwt));
-  Sd = ff_mul_f(Sd, part_scale(Cd, Cwd));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const ff a = ff_shfl_xor(St, o), b = ff_shfl_xor(Sd, o);
-    St = ff_add(St, a);
-    Sd = ff_add(Sd, b);
-  }
-  Ct = Cwt;
-  Cd = Cwd;
-}
+// partial sums carry integer reference points (sv_common.cuh): rescales are
+// exact powers of two
+__device__ __forceinline__ float part_scale(float c, float C) { return scale_exact(c, C); }
 // r(y) (mode 0: max(p - q, 0); mode 1: p) from fp32 logits.  The masses and
 // the final walk evaluate it with identical operations, so they see
 // bit-identical values.
@@ -544,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 3) dense_fused_kernel(const __grid_c
   // the latest word on earlier rejections of this row (a hint; rank 0's copy
   // is the one every rank uses), read as late as possible
   if (tid == 0 && rank == 0) hint = ldcg_u32(P.rej + b);
-  warp_combine2(Ct, St, Cd, Sd);
+  warp_combine_pair(Ct, St, Cd, Sd);
   if (lane == 0) {
     uint32_t txb = kNoTokenBits, dxb = kNoTokenBits;
     const int xl = xj - y0;

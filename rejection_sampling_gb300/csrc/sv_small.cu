@@ -104,6 +104,24 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
     if (lane < R && __popc(same) > 1) bad = 1;
   }
   bad = __any_sync(0xffffffffu, bad);
+  // the row's small inputs, issued now so their latency hides behind the
+  // staging: lane i's accept uniform and draft token (any-order: the token at
+  // sigma_i; when the whole sequence is the window it is read in position
+  // order and moved to lane i by a shuffle), and the sample uniform
+  const bool xin = P.anyorder && P.D <= 32;
+  int xsrc = 0;
+  float uacc = 1.f;
+  if (lane < NT) uacc = P.u_acc[(size_t)b * NT + lane];
+  if (P.anyorder) {
+    if (xin) {
+      if (lane < P.D) xsrc = P.x[(size_t)b * P.D + lane];
+    } else if (lane < R && !bad) {
+      xsrc = P.x[(size_t)b * P.D + sig];
+    }
+  } else if (lane < NT) {
+    xsrc = P.x[(size_t)b * NT + lane];
+  }
+  const float usamp = P.u_s[b];
 
   // ---- stage the rows in shared memory (row r of the warp = position r) ----
   // The R x V block is walked flat, 32 consecutive elements per step, so every
@@ -217,13 +235,14 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
       }
     }
   }
+  if (xin) x = __shfl_sync(0xffffffffu, xsrc, (sig >= 0 && sig < 32) ? sig : 0);
+  else x = xsrc;
   if (!bad && lane < R) {
     if (!by_warp) row_stats(st + prow * VS, V, ct, St);
     err |= !stats_ok(ct, St);
     if (lane < NT) {
       if (!by_warp) row_stats(sd + prow * VS, V, cd, Sd);
       err |= !stats_ok(cd, Sd);
-      x = P.anyorder ? P.x[(size_t)b * P.D + sig] : P.x[(size_t)b * NT + lane];
       if (x < 0 || x >= V) err = 1;
       if (!err) {
         const float tx = st[prow * VS + x], dx = sd[prow * VS + x];
@@ -235,7 +254,7 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
           ratio = exp2f(ff_to_f(ff_sub(ea, ed))) * __fdiv_rn(Sd, St);
         }
         a = fminf(ratio, 1.f);
-        acc = P.u_acc[(size_t)b * NT + lane] < a;
+        acc = uacc < a;
       }
     }
   }
@@ -270,7 +289,7 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
         mode = 1;
         continue;
       }
-      const ff target = ff_mul_f(T, P.u_s[b]);
+      const ff target = ff_mul_f(T, usamp);
       const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(ex, ls), target));
       if (hit) {
         const int fl = __ffs(hit) - 1;
@@ -333,11 +352,43 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
 
 size_t small_smem_per_warp(int R, int vstride) { return (size_t)2 * R * vstride * sizeof(float); }
 
+// Warps per CTA for a per-warp shared-memory need: the count (at most 12)
+// that keeps the most warps resident per SM, given the SM's shared memory,
+// the per-block reservation and the register file (e.g. 9 warps of 8.25 KB:
+// 3 CTAs, 27 warps per SM, so 4096 sequences take one wave on 152 SMs).
+int small_warps_per_cta(size_t per) {
+  static int cap = 0, resv = 0, maxblk = 0;
+  if (cap == 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&cap, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&resv, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&maxblk, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cap = 0;
+      return 8;
+    }
+  }
+  cudaFuncAttributes fa;
+  const int regs = (cudaFuncGetAttributes(&fa, small_verify_kernel) == cudaSuccess && fa.numRegs > 0)
+                       ? fa.numRegs : 64;
+  const int reg_warps = 65536 / (regs * 32);
+  int best = 1, best_res = 0;
+  for (int w = 1; w <= 12; ++w) {
+    const size_t blk = per * w;
+    if (blk > (size_t)maxblk) break;
+    int ctas = (int)(cap / (blk + resv));
+    ctas = min(ctas, reg_warps / w);
+    if (ctas * w > best_res) {
+      best_res = ctas * w;
+      best = w;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_small(const SmallParams& p, cudaStream_t s) {
   const size_t per = small_smem_per_warp(p.R, p.vstride);
-  int warps = (int)((96 * 1024) / per);
-  if (warps > 8) warps = 8;
-  if (warps < 1) warps = 1;
+  const int warps = small_warps_per_cta(per);
   const size_t smem = per * warps;
   if (smem > 48 * 1024) {
     cudaError_t e =

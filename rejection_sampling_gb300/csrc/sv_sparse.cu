@@ -11,50 +11,69 @@
 // position gamma (same guide, section 2).
 //
 // One CTA per row, one warp per position (gamma + 1 <= 32 warps).  Warp j
-// validates its lists and runs its accept test; a shared-memory scan finds
-// the first rejection n; warp n then merges its target list against the
-// sorted draft list (binary search per target id), scans the residual in float-float
-// in list order and draws the token.
+// issues its small loads first, validates its lists (copying a draft list of
+// up to kStageK entries into shared memory as it goes) and runs its accept
+// test; a shared-memory scan finds the first rejection n; warp n then finds
+// each target id's draft probability by binary search in the staged draft
+// list (in global memory for longer lists), scans the residual in
+// float-float in list order and draws the token.
 #include "sv_common.cuh"
 
 namespace sv {
 namespace {
 
+constexpr int kStageK = 128;  // draft lists up to this length are staged in shared memory
+
+// A list is valid if its ids are in [0, V) and strictly ascending and its
+// probabilities finite and >= 0; with `sid` / `sp` it is also copied there.
 __device__ __forceinline__ bool list_ok(const int32_t* ids, const float* pr, int k, int V,
-                                        int lane) {
+                                        int lane, int32_t* sid = nullptr, float* sp = nullptr) {
   bool ok = true;
   for (int i = lane; i < k; i += 32) {
     const int id = ids[i];
-    if (id < 0 || id >= V) ok = false;
-    if (i + 1 < k && ids[i + 1] <= id) ok = false;
+    const int nx = (i + 1 < k) ? ids[i + 1] : 0x7fffffff;
     const float p = pr[i];
+    if (id < 0 || id >= V) ok = false;
+    if (nx <= id) ok = false;
     if (!(p >= 0.f) || p == INFINITY) ok = false;
+    if (sid) {
+      sid[i] = id;
+      sp[i] = p;
+    }
   }
   return __all_sync(0xffffffffu, ok);
 }
 
-// probability of `id` in a sorted list (0 if absent)
+// probability of `id` in a sorted list (0 if absent), in shared or global memory
 __device__ __forceinline__ float list_lookup(const int32_t* ids, const float* pr, int k, int id) {
   int lo = 0, hi = k;
   while (lo < hi) {
     const int mid = (lo + hi) >> 1;
-    const int v = __ldg(ids + mid);
+    const int v = ids[mid];
     if (v < id)
       lo = mid + 1;
     else
       hi = mid;
   }
-  return (lo < k && __ldg(ids + lo) == id) ? __ldg(pr + lo) : 0.f;
+  return (lo < k && ids[lo] == id) ? pr[lo] : 0.f;
 }
 
 __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   __shared__ int s_acc[32];
   __shared__ int s_err[32];
   __shared__ int s_n;
+  extern __shared__ __align__(16) unsigned char s_lists[];  // G x kStageK (id, prob) when staged
   const int b = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = P.G, kt = P.kt, kd = P.kd, V = P.V;
   const int32_t* tid = P.tid + ((size_t)b * (G + 1) + j) * kt;
   const float* tp = P.tp + ((size_t)b * (G + 1) + j) * kt;
+  const bool staged = kd <= kStageK;
+  int32_t* sid = reinterpret_cast<int32_t*>(s_lists) + (size_t)j * kStageK;
+  float* sdp = reinterpret_cast<float*>(s_lists + (size_t)G * kStageK * sizeof(int32_t)) + (size_t)j * kStageK;
+  // small inputs first: their latency hides behind the list loads
+  const int x = (j < G) ? P.x[(size_t)b * G + j] : 0;
+  const float uj = (j < G) ? P.u_acc[(size_t)b * G + j] : 0.f;
+  const float us = P.u_s[b];
 
   bool err = !list_ok(tid, tp, kt, V, lane);
   int acc = 1;
@@ -62,8 +81,7 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   if (j < G) {
     const int32_t* did = P.did + ((size_t)b * G + j) * kd;
     const float* dp = P.dp + ((size_t)b * G + j) * kd;
-    err |= !list_ok(did, dp, kd, V, lane);
-    const int x = P.x[(size_t)b * G + j];
+    err |= staged ? !list_ok(did, dp, kd, V, lane, sid, sdp) : !list_ok(did, dp, kd, V, lane);
     if (x < 0 || x >= V) err = true;
     float ps = 0.f, qs = 0.f;
     for (int i = lane; i < kt; i += 32)
@@ -74,7 +92,7 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
     qs = warp_sum(qs);
     const float ratio = (qs > 0.f) ? __fdiv_rn(ps, qs) : 0.f;
     a = fminf(ratio, 1.f);
-    acc = P.u_acc[(size_t)b * G + j] < a;
+    acc = uj < a;
   }
   if (lane == 0) {
     s_acc[j] = acc;
@@ -107,8 +125,11 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   if (j != n) return;
 
   // ---- warp n: residual on the target support (or the bonus list) ----
-  const int32_t* did = (n < G) ? P.did + ((size_t)b * G + n) * kd : nullptr;
-  const float* dp = (n < G) ? P.dp + ((size_t)b * G + n) * kd : nullptr;
+  // the draft list of position n: as staged by this warp (shared memory) or in
+  // global memory
+  __syncwarp();
+  const int32_t* did = (n < G) ? (staged ? sid : P.did + ((size_t)b * G + n) * kd) : nullptr;
+  const float* dp = (n < G) ? (staged ? sdp : P.dp + ((size_t)b * G + n) * kd) : nullptr;
   const int q = (kt + 31) / 32;
   const int e0 = min(kt, lane * q), e1 = min(kt, e0 + q);
   int mode = (n < G) ? 0 : 1;
@@ -132,7 +153,7 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   }
   int yi = -1;
   if (T.hi > 0.f) {
-    const ff target = ff_mul_f(T, P.u_s[b]);
+    const ff target = ff_mul_f(T, us);
     const unsigned hit = __ballot_sync(0xffffffffu, (e1 > e0) && ff_gt(ff_add(ex, ls), target));
     if (hit) {
       const int fl = __ffs(hit) - 1;
@@ -171,7 +192,9 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
 }  // namespace
 
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
-  sparse_verify_kernel<<<p.B, 32 * (p.G + 1), 0, s>>>(p);
+  // G x kStageK x 8 bytes <= 31 KB: within the default dynamic shared memory
+  const size_t smem = (p.kd <= kStageK) ? (size_t)p.G * kStageK * (sizeof(int32_t) + sizeof(float)) : 0;
+  sparse_verify_kernel<<<p.B, 32 * (p.G + 1), smem, s>>>(p);
   return cudaGetLastError();
 }
 
