@@ -392,11 +392,16 @@ struct ConfRec {  // one segment (32 bytes, at the segment's first piece slot)
   int pad[2];
 };
 
+// A segment's running statistics, per lane: the lane's maximum, the first
+// id holding it, an integer reference point c >= log2e * max and the sum
+// S = sum 2^(v log2e - c) of the lane's elements (float-float); the lanes are
+// combined once, when the warp's range leaves the segment.
 struct CSeg {
   long long w0;
   int b, j;
-  float m;
-  ff S;
+  float m;  // this lane's maximum
+  float c;  // this lane's reference point
+  ff S;     // this lane's sum, relative to c
   int idx, bad;
   bool live;  // the position is masked (a record will be written)
 };
@@ -447,49 +452,96 @@ __device__ __forceinline__ void cseg_begin(CSeg& s, const DenseParams& P, const 
   s.b = it.b;
   s.j = it.j;
   s.m = -INFINITY;
+  s.c = -INFINITY;
   s.S = ff{0.f, 0.f};
   s.idx = INT_MAX;
   s.bad = 0;
   s.live = is_masked(P, it.b, it.j);
 }
+// every lane: the lanes are combined -- the maximum, the smallest first id
+// among the lanes holding it, the sums moved exactly to the largest reference
+// point and added, then expressed relative to the maximum (one exp2f) -- and
+// lane 0 writes the record
 __device__ __forceinline__ void cseg_write(const DenseParams& P, const CSeg& s, int lane) {
-  if (lane == 0 && s.live) {
+  if (!s.live) return;
+  const int bad = __any_sync(0xffffffffu, s.bad);
+  const float M = ord2f(__reduce_max_sync(0xffffffffu, f2ord(s.m)));
+  const int idx = (int)__reduce_min_sync(0xffffffffu, (unsigned)((s.m == M && !bad) ? s.idx : INT_MAX));
+  const float C = ord2f(__reduce_max_sync(0xffffffffu, f2ord(s.c)));
+  ff S = warp_sum_ff(ff_mul_f(s.S, scale_exact(s.c, C)));
+  if (M > -INFINITY && !bad) S = ff_mul_f(S, exp2f(C - M * kLog2e));
+  if (lane == 0) {
     int4* q = reinterpret_cast<int4*>(reinterpret_cast<ConfRec*>(P.ws + P.L.upart) + s.w0);
-    q[0] = make_int4(__float_as_int(s.m), __float_as_int(s.S.hi), __float_as_int(s.S.lo), s.idx);
-    q[1] = make_int4(s.bad, 1, 0, 0);  // .y = 1 marks a record
+    q[0] = make_int4(__float_as_int(M), __float_as_int(S.hi), __float_as_int(S.lo), idx);
+    q[1] = make_int4(bad, 1, 0, 0);  // .y = 1 marks a record
   }
 }
-// (max, sum, first id, bad) of a piece folded into the segment (pieces in
-// increasing id order: a strictly greater maximum takes over, ties keep it)
+// This lane's elements of a piece folded into its segment statistics.  The
+// lane's elements come in increasing id order (pieces in order; in a piece,
+// vectors lane + 32 i, elements in order), so a strictly greater maximum takes
+// over and ties keep the earlier id; the first id is searched only when the
+// lane's maximum grows.  A NaN or +inf marks the lane bad.
 __device__ __forceinline__ void cseg_add(CSeg& s, const CItem& it, const uint4 (&r)[4], int bf16,
                                          int pe, int lane) {
-  float m;
-  int idx, bad;
-  piece_argmax(r, bf16, lane, m, idx, bad);
-  s.bad |= bad;
-  if (bad || m == -INFINITY) return;  // nothing to add (a bad segment is an error anyway)
-  const float c = m * kLog2e;
+  if (s.bad) return;  // the segment is an error; nothing more to add
+  float pm;
+  if (bf16) {
+    uint32_t mx = kNegInf2;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      mx = bf16x2_max_nan(mx, bf16x2_max_nan(bf16x2_max_nan(r[i].x, r[i].y),
+                                             bf16x2_max_nan(r[i].z, r[i].w)));
+    pm = fmax_nan(bf16_lo(mx), bf16_hi(mx));
+  } else {
+    pm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      pm = fmax_nan(pm, fmax_nan(fmax_nan(__uint_as_float(r[i].x), __uint_as_float(r[i].y)),
+                                 fmax_nan(__uint_as_float(r[i].z), __uint_as_float(r[i].w))));
+  }
+  if (pm != pm || pm == INFINITY) {
+    s.bad = 1;
+    return;
+  }
+  if (pm == -INFINITY) return;
+  if (pm > s.m) {  // a new maximum for this lane: its first id, then the reference point
+    int bi = INT_MAX;
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {  // scanned backwards, so the last hit is the first id
+      const uint32_t w[4] = {r[i].x, r[i].y, r[i].z, r[i].w};
+      if (bf16) {
+#pragma unroll
+        for (int e = 7; e >= 0; --e)
+          if (((e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1])) == pm) bi = (lane + 32 * i) * 8 + e;
+      } else {
+#pragma unroll
+        for (int e = 3; e >= 0; --e)
+          if (__uint_as_float(w[e]) == pm) bi = (lane + 32 * i) * 4 + e;
+      }
+    }
+    s.m = pm;
+    s.idx = it.k * pe + bi;
+    const float c = ref_point(pm);
+    if (c > s.c) {
+      s.S = ff_mul_f(s.S, scale_exact(s.c, c));
+      s.c = c;
+    }
+  }
+  const float cc = s.c;
   float a0 = 0.f, a1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (bf16) {
-      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].x), kLog2e, -c));
-      a1 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].y), kLog2e, -c));
-      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].z), kLog2e, -c));
-      a1 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -c)) + ex2(fmaf(bf16_hi(r[i].w), kLog2e, -c));
+      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].x), kLog2e, -cc));
+      a1 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].y), kLog2e, -cc));
+      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].z), kLog2e, -cc));
+      a1 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].w), kLog2e, -cc));
     } else {
-      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -c)) + ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -c));
-      a1 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -c)) + ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -c));
+      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -cc)) + ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -cc));
+      a1 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -cc)) + ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -cc));
     }
   }
-  const float ps = warp_sum(a0 + a1);
-  if (m > s.m) {
-    s.S = ff_add(ff_mul_f(s.S, (s.m == -INFINITY) ? 0.f : ex2(s.m * kLog2e - c)), ff{ps, 0.f});
-    s.m = m;
-    s.idx = it.k * pe + idx;
-  } else {
-    s.S = ff_add(s.S, two_prod(ps, ex2(c - s.m * kLog2e)));
-  }
+  s.S = ff_add_f(s.S, a0 + a1);
 }
 
 __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid_constant__ DenseParams P) {

@@ -368,9 +368,12 @@ int small_warps_per_cta(size_t per) {
       return 8;
     }
   }
-  cudaFuncAttributes fa;
-  const int regs = (cudaFuncGetAttributes(&fa, small_verify_kernel) == cudaSuccess && fa.numRegs > 0)
-                       ? fa.numRegs : 64;
+  static int regs = 0;  // the kernel's registers per thread, asked once
+  if (regs == 0) {
+    cudaFuncAttributes fa;
+    regs = (cudaFuncGetAttributes(&fa, small_verify_kernel) == cudaSuccess && fa.numRegs > 0) ? fa.numRegs
+                                                                                              : 64;
+  }
   const int reg_warps = 65536 / (regs * 32);
   int best = 1, best_res = 0;
   for (int w = 1; w <= 12; ++w) {
