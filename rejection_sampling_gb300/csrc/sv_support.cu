@@ -467,7 +467,7 @@ __device__ __forceinline__ void read_chunk(const unsigned char* d, const unsigne
 }
 
 template <int NPL, int W>
-__global__ void __launch_bounds__(32 * W, 3)
+__global__ void __launch_bounds__(32 * W, (W <= 3) ? 8 : ((W <= 6) ? 4 : 3))
     support_kernel(const __grid_constant__ SupportParams P) {
   constexpr int kCap = key_cap<NPL>();
   constexpr int kGCap = gather_cap<NPL>();
@@ -713,20 +713,24 @@ cudaError_t launch_support(const unsigned char* lt, int N, int V, int K, int bf1
   p.ids = ids;
   p.probs = probs;
   p.status = status;
-  // 8 warps and about 67 KB of shared memory (K <= 64) per row: 3 rows per SM
+  // K <= 64: 6 warps and about 51 KB of shared memory per row, 4 rows per SM
+  // (measured 66.3 us against 68.2 us with 8 warps and 3 rows per SM for 960
+  // rows of 128256 bf16 logits; 3 warps and 8 rows per SM took 98.7 us: the
+  // per-row phases outside the stream lengthen); larger K: 8 warps
   const size_t ring = (size_t)8 * kRStages * kChunkB;
+  const size_t ring6 = (size_t)6 * kRStages * kChunkB;
   static bool attr[64] = {false};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && !attr[dev]) {
     const int carve = cudaSharedmemCarveoutMaxShared;
-    e = cudaFuncSetAttribute(support_kernel<1, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<2, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+    e = cudaFuncSetAttribute(support_kernel<1, 6>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<2, 6>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<1, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring6);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<2, 6>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring6);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<4, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<8, 8>, cudaFuncAttributePreferredSharedMemoryCarveout, carve);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<1, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<2, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<4, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(support_kernel<8, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ring);
     if (e != cudaSuccess) return e;
@@ -742,8 +746,12 @@ cudaError_t launch_support(const unsigned char* lt, int N, int V, int K, int bf1
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (K <= 32) return cudaLaunchKernelEx(&cfg, support_kernel<1, 8>, p);
-  if (K <= 64) return cudaLaunchKernelEx(&cfg, support_kernel<2, 8>, p);
+  if (K <= 64) {
+    cfg.blockDim = dim3(6 * 32, 1, 1);
+    cfg.dynamicSmemBytes = ring6;
+    if (K <= 32) return cudaLaunchKernelEx(&cfg, support_kernel<1, 6>, p);
+    return cudaLaunchKernelEx(&cfg, support_kernel<2, 6>, p);
+  }
   if (K <= 128) return cudaLaunchKernelEx(&cfg, support_kernel<4, 8>, p);
   return cudaLaunchKernelEx(&cfg, support_kernel<8, 8>, p);
 }
