@@ -87,9 +87,9 @@ __device__ __forceinline__ float load_logit(const unsigned char* row, int y, int
 }
 
 // fp32 scale 2^(c - C) for combining partial sums (0 for an all -inf part)
-__device__ __forceinline__ float part_scale(float c, float C) {
-  return (c == -INFINITY) ? 0.f : exp2f(c - C);
-}
+// (the statistics records carry integer reference points, so this is an
+// exact power of two formed on the integer pipe)
+__device__ __forceinline__ float part_scale(float c, float C) { return scale_exact(c, C); }
 
 // r(y) from fp32 logits; identical operations wherever it is evaluated so the
 // masses and the final walk see bit-identical values.
@@ -328,12 +328,6 @@ __device__ __forceinline__ void combine_part(const UnitPart& u, float& Ct, ff& S
   }
 }
 
-// warp-wide combination of per-lane (C, S) pairs
-__device__ __forceinline__ void warp_combine(float& C, ff& S) {
-  const float Cw = warp_max(C);
-  S = warp_sum_ff(ff_mul_f(S, part_scale(C, Cw)));
-  C = Cw;
-}
 
 struct FinShared {
   float c[4][kMaxG];  // per position: Ct, St, Cd, Sd (the stop position's constants)
@@ -356,6 +350,10 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
   // the statistics grid gave warp g the pieces [lo(g), lo(g + 1)), lo(g) =
   // g W / nwt; a segment record sits at the first piece of the segment
   const long long W = (long long)P.B * (G + 1) * np, nwt = P.stats_warps;
+  // the range arithmetic in 32 bits when every product fits (a 64-bit
+  // division is a long software sequence on the critical path of every row)
+  const bool idx32 = (unsigned long long)(nwt + 1) * (unsigned long long)(W + 1) < (1ull << 32);
+  const unsigned W32 = (unsigned)W, n32 = (unsigned)nwt;
   if (threadIdx.x == 0) {
     F.n = G + 1;
     F.err = 0;
@@ -367,9 +365,13 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     uint32_t txb = kNoTokenBits, dxb = kNoTokenBits;
     const long long P0 = ((long long)b * (G + 1) + j) * np, P1 = P0 + np;
     // warps whose ranges meet [P0, P1): lo(g) <= P0 for the first, lo(g) < P1 for the last
-    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    const long long g0 = idx32 ? (long long)(((unsigned)(P0 + 1) * n32 + W32 - 1) / W32) - 1
+                               : ((P0 + 1) * nwt + W - 1) / W - 1;
+    const long long g1 = idx32 ? (long long)(((unsigned)P1 * n32 + W32 - 1) / W32) - 1
+                               : (P1 * nwt + W - 1) / W - 1;
     for (long long g = g0 + lane; g <= g1; g += 32) {
-      const long long lo = g * W / nwt, lo1 = (g + 1) * W / nwt;
+      const long long lo = idx32 ? (long long)((unsigned)g * W32 / n32) : g * W / nwt;
+      const long long lo1 = idx32 ? (long long)((unsigned)(g + 1) * W32 / n32) : (g + 1) * W / nwt;
       if (lo1 <= lo) continue;  // an empty range writes nothing
       const UnitPart u = ldcg32(rec + (lo > P0 ? lo : P0));
       combine_part(u, Ct, St, Cd, Sd);
@@ -378,8 +380,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
         dxb = __float_as_uint(u.dx);
       }
     }
-    warp_combine(Ct, St);
-    warp_combine(Cd, Sd);
+    warp_combine_pair(Ct, St, Cd, Sd);
     const unsigned hx = __ballot_sync(0xffffffffu, txb != kNoTokenBits);
     if (hx) {
       txb = __shfl_sync(0xffffffffu, txb, __ffs(hx) - 1);
