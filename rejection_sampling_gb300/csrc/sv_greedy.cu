@@ -314,14 +314,22 @@ __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __gri
   // the statistics grid gave warp g the pieces [lo(g), lo(g + 1)), lo(g) =
   // g W / nwt; a segment record sits at the first piece of each segment
   const long long W = (long long)P.B * (G + 1) * np, nwt = P.stats_warps;
+  // the range arithmetic in 32 bits when every product fits (a 64-bit
+  // division is a long software sequence on each row's critical path)
+  const bool idx32 = (unsigned long long)(nwt + 1) * (unsigned long long)(W + 1) < (1ull << 32);
+  const unsigned W32 = (unsigned)W, n32 = (unsigned)nwt;
   for (int j = warp; j <= G; j += kGRowWarps) {
     const int xj = (j < G) ? P.x[(size_t)b * G + j] : 0;
     const long long P0 = ((long long)b * (G + 1) + j) * np, P1 = P0 + np;
-    const long long g0 = ((P0 + 1) * nwt + W - 1) / W - 1, g1 = (P1 * nwt + W - 1) / W - 1;
+    const long long g0 = idx32 ? (long long)(((unsigned)(P0 + 1) * n32 + W32 - 1) / W32) - 1
+                               : ((P0 + 1) * nwt + W - 1) / W - 1;
+    const long long g1 = idx32 ? (long long)(((unsigned)P1 * n32 + W32 - 1) / W32) - 1
+                               : (P1 * nwt + W - 1) / W - 1;
     float m = -INFINITY;
     int idx = INT_MAX, bad = 0;
     for (long long g = g0 + lane; g <= g1; g += 32) {
-      const long long l0 = g * W / nwt, l1 = (g + 1) * W / nwt;
+      const long long l0 = idx32 ? (long long)((unsigned)g * W32 / n32) : g * W / nwt;
+      const long long l1 = idx32 ? (long long)((unsigned)(g + 1) * W32 / n32) : (g + 1) * W / nwt;
       if (l1 <= l0) continue;  // an empty range writes nothing
       int4* rp = reinterpret_cast<int4*>(rec + (l0 > P0 ? l0 : P0));
       const int4 v = __ldcg(rp);
