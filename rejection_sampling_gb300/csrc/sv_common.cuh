@@ -42,6 +42,41 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
 }
 
 // ---------------------------------------------------------------------------
+// packed fp32 pairs (add / fma .f32x2 on a 64-bit register pair): one issue
+// slot for two round-to-nearest operations, each rounded exactly as the
+// scalar instruction would round it
+// ---------------------------------------------------------------------------
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 f2_pack(float a, float b) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(f32x2 r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ f32x2 f2_add(f32x2 a, f32x2 b) {
+  f32x2 d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// (2^(a0 L - c), 2^(a1 L - c)) for the pair (a0, a1): one packed fma, two ex2
+__device__ __forceinline__ f32x2 f2_exp2_shift(f32x2 a, f32x2 L, f32x2 nc) {
+  float y0, y1;
+  f2_unpack(f2_fma(a, L, nc), y0, y1);
+  return f2_pack(ex2(y0), ex2(y1));
+}
+// a bf16 pair in one 32-bit word as an fp32 pair (exact)
+__device__ __forceinline__ f32x2 f2_bf16(uint32_t w) {
+  return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// ---------------------------------------------------------------------------
 // warp reductions
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

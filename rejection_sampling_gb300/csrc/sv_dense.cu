@@ -184,29 +184,28 @@ __device__ __forceinline__ void lane_fold(const uint4 (&r)[4], int bf16, float& 
     C = c;
   }
   const float cc = (C == -INFINITY) ? 0.f : C;
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  // four running sums a0..a3 as two packed pairs: (a0, a1) and (a2, a3)
+  const f32x2 L2 = f2_pack(kLog2e, kLog2e), nc = f2_pack(-cc, -cc);
+  f32x2 a01 = f2_pack(0.f, 0.f), a23 = a01;
   if (bf16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -cc));
-      a1 += ex2(fmaf(bf16_hi(r[i].x), kLog2e, -cc));
-      a2 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -cc));
-      a3 += ex2(fmaf(bf16_hi(r[i].y), kLog2e, -cc));
-      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -cc));
-      a1 += ex2(fmaf(bf16_hi(r[i].z), kLog2e, -cc));
-      a2 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -cc));
-      a3 += ex2(fmaf(bf16_hi(r[i].w), kLog2e, -cc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].x), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].y), L2, nc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].z), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].w), L2, nc));
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -cc));
-      a1 += ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -cc));
-      a2 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -cc));
-      a3 += ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -cc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_pack(__uint_as_float(r[i].x), __uint_as_float(r[i].y)), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_pack(__uint_as_float(r[i].z), __uint_as_float(r[i].w)), L2, nc));
     }
   }
-  S = ff_add_f(S, (a0 + a1) + (a2 + a3));
+  float a0, a1, a2, a3;
+  f2_unpack(a01, a0, a1);
+  f2_unpack(a23, a2, a3);
+  S = ff_add_f(S, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
 }
 
 // fp32 bits of element xl (0 <= xl < ne) of the piece, on every lane
