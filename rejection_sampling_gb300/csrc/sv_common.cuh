@@ -77,6 +77,17 @@ __device__ __forceinline__ f32x2 f2_bf16(uint32_t w) {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may be scheduled while its predecessor on the stream is still
+// running; this waits until that grid has completed (and its memory is
+// visible) before anything is read, then lets the next grid be scheduled
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait_then_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // warp reductions
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_max(float v) {

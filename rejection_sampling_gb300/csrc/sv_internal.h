@@ -217,6 +217,22 @@ struct SparseParams {
   int B, G, V, kt, kd;
 };
 
+// a launch configuration with programmatic stream serialisation (the kernel
+// starts with griddepcontrol.wait); `attr` holds the one attribute
+inline cudaLaunchConfig_t pdl_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                     cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t c = {};
+  c.gridDim = grid;
+  c.blockDim = block;
+  c.dynamicSmemBytes = smem;
+  c.stream = s;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  c.attrs = attr;
+  c.numAttrs = 1;
+  return c;
+}
+
 // launchers (return the CUDA error of the launch)
 // the two dense kernels (statistics + row decisions, then residual + draw)
 cudaError_t launch_dense(const DenseParams& p, cudaStream_t s);

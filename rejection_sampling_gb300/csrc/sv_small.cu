@@ -86,6 +86,7 @@ __device__ __forceinline__ bool stats_ok(float c, float s) {
 
 __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   extern __shared__ float smem[];
+  pdl_wait_then_release();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + warp;
   if (b >= P.B) return;  // whole warp leaves; no block-wide barrier below
@@ -399,8 +400,9 @@ cudaError_t launch_small(const SmallParams& p, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   const long long blocks = ((long long)p.B + warps - 1) / warps;
-  small_verify_kernel<<<(unsigned)blocks, warps * 32, smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute a[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3((unsigned)blocks), dim3(warps * 32), smem, s, a);
+  return cudaLaunchKernelEx(&cfg, small_verify_kernel, p);
 }
 
 }  // namespace sv

@@ -63,6 +63,7 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
   __shared__ int s_err[32];
   __shared__ int s_n;
   extern __shared__ __align__(16) unsigned char s_lists[];  // G x kStageK (id, prob) when staged
+  pdl_wait_then_release();
   const int b = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = P.G, kt = P.kt, kd = P.kd, V = P.V;
   const int32_t* tid = P.tid + ((size_t)b * (G + 1) + j) * kt;
@@ -194,8 +195,9 @@ __global__ void sparse_verify_kernel(const __grid_constant__ SparseParams P) {
 cudaError_t launch_sparse(const SparseParams& p, cudaStream_t s) {
   // G x kStageK x 8 bytes <= 31 KB: within the default dynamic shared memory
   const size_t smem = (p.kd <= kStageK) ? (size_t)p.G * kStageK * (sizeof(int32_t) + sizeof(float)) : 0;
-  sparse_verify_kernel<<<p.B, 32 * (p.G + 1), smem, s>>>(p);
-  return cudaGetLastError();
+  cudaLaunchAttribute a[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(p.B), dim3(32 * (p.G + 1)), smem, s, a);
+  return cudaLaunchKernelEx(&cfg, sparse_verify_kernel, p);
 }
 
 }  // namespace sv
