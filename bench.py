@@ -215,8 +215,9 @@ def time_prepared(calls, stream, iters):
     return e0.elapsed_time(e1) / iters
 
 
-def variant_lines(dev, stream):
-    """Kernel time of the other workloads (each call timed back to back)."""
+def variant_lines(dev, stream, only=None):
+    """Kernel time of the other workloads (each call timed back to back);
+    `only`: the line names to run (all when None)."""
     import numpy as np
     import torch
     import rejection_sampling_gb300 as rs
@@ -233,6 +234,8 @@ def variant_lines(dev, stream):
             ("support_b64_g7_v128256", "support_b64_g7_v128256", None),
             ("rounds_b4096_r4_d256_v27", "rounds_b4096_r4_d256_v27", None)]
     for name, wname, forced in runs:
+        if only is not None and name not in only:
+            continue
         d = wl.make(wname, seed=0)
         if forced:
             os.environ[PATH_ENV] = forced

@@ -135,13 +135,17 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
     const int nt = (P.anyorder ? P.D : NT + 1) * V / 4, nd = (P.anyorder ? P.D : NT) * V / 4;
     const float4* ts = reinterpret_cast<const float4*>(P.lt) + (size_t)b * nt;
     const float4* ds = reinterpret_cast<const float4*>(P.ld) + (size_t)b * nd;
+    // two copy groups: the target block, then the draft block -- the target
+    // statistics run while the draft block is still arriving
     for (int i = lane; i < nt; i += 32)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(st + 4 * i)), "l"(ts + i)
                    : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
     for (int i = lane; i < nd; i += 32)
       asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sd + 4 * i)), "l"(ds + i)
                    : "memory");
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
   } else {
     const int total = R * V;
     int r = lane / V, y = lane - (lane / V) * V;  // (row, column) of element `lane`
@@ -224,6 +228,10 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   // their count; for few long rows the whole warp takes one row at a time
   // (about R * (V / 32 + 20) steps instead of V).
   const bool by_warp = R * (V + 640) < 32 * V;
+  if (P.flat && by_warp) {  // the warp-wide statistics read both blocks at once
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
   if (!bad && by_warp) {
     for (int r = 0; r < R; ++r) {
       const int rr = (P.flat && P.anyorder) ? __shfl_sync(0xffffffffu, sig, r) : r;
@@ -238,8 +246,12 @@ __global__ void small_verify_kernel(const __grid_constant__ SmallParams P) {
   }
   if (xin) x = __shfl_sync(0xffffffffu, xsrc, (sig >= 0 && sig < 32) ? sig : 0);
   else x = xsrc;
+  if (!bad && lane < R && !by_warp) row_stats(st + prow * VS, V, ct, St);
+  if (P.flat && !by_warp) {  // the draft block's copy group
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
   if (!bad && lane < R) {
-    if (!by_warp) row_stats(st + prow * VS, V, ct, St);
     err |= !stats_ok(ct, St);
     if (lane < NT) {
       if (!by_warp) row_stats(sd + prow * VS, V, cd, Sd);
