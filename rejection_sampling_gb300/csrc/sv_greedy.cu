@@ -419,6 +419,12 @@ __device__ __forceinline__ bool is_masked(const DenseParams& P, int b, int j) {
 }
 
 constexpr int kCMaxList = 8192;  // positions whose masked subset is listed in shared memory
+// The commit statistics kernel's geometry (the greedy sweep's: measured
+// against 12 x 8, 16 x 6 and 24 x 4 warps x stages, all slower)
+constexpr int kCWarps = 24;
+constexpr int kCThreads = 32 * kCWarps;
+constexpr int kCStages = 3;  // 2 KB stages per warp
+constexpr size_t kCSmem = (size_t)kCWarps * kCStages * kPieceBytes;
 
 // Pieces in the order the statistics warps sweep them: every piece of the
 // batch (all = 1), or only the pieces of masked positions, position list[m]
@@ -536,26 +542,31 @@ __device__ __forceinline__ void cseg_add(CSeg& s, const CItem& it, const uint4 (
     }
   }
   const float cc = s.c;
-  float a0 = 0.f, a1 = 0.f;
+  // four running sums as two packed pairs (one fma and one add per pair)
+  const f32x2 L2 = f2_pack(kLog2e, kLog2e), nc = f2_pack(-cc, -cc);
+  f32x2 a01 = f2_pack(0.f, 0.f), a23 = a01;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (bf16) {
-      a0 += ex2(fmaf(bf16_lo(r[i].x), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].x), kLog2e, -cc));
-      a1 += ex2(fmaf(bf16_lo(r[i].y), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].y), kLog2e, -cc));
-      a0 += ex2(fmaf(bf16_lo(r[i].z), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].z), kLog2e, -cc));
-      a1 += ex2(fmaf(bf16_lo(r[i].w), kLog2e, -cc)) + ex2(fmaf(bf16_hi(r[i].w), kLog2e, -cc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].x), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].y), L2, nc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].z), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].w), L2, nc));
     } else {
-      a0 += ex2(fmaf(__uint_as_float(r[i].x), kLog2e, -cc)) + ex2(fmaf(__uint_as_float(r[i].y), kLog2e, -cc));
-      a1 += ex2(fmaf(__uint_as_float(r[i].z), kLog2e, -cc)) + ex2(fmaf(__uint_as_float(r[i].w), kLog2e, -cc));
+      a01 = f2_add(a01, f2_exp2_shift(f2_pack(__uint_as_float(r[i].x), __uint_as_float(r[i].y)), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift(f2_pack(__uint_as_float(r[i].z), __uint_as_float(r[i].w)), L2, nc));
     }
   }
-  s.S = ff_add_f(s.S, a0 + a1);
+  float a0, a1, a2, a3;
+  f2_unpack(a01, a0, a1);
+  f2_unpack(a23, a2, a3);
+  s.S = ff_add_f(s.S, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
 }
 
-__global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid_constant__ DenseParams P) {
+__global__ void __launch_bounds__(kCThreads, 1) commit_stats_kernel(const __grid_constant__ DenseParams P) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ int s_list[kCMaxList];
-  __shared__ int s_wsum[kGWarps];
+  __shared__ int s_wsum[kCWarps];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = P.G, Wn = G + 1, np = P.g.np, pe = P.g.pe, epv = P.bf16 ? 8 : 4;
@@ -564,7 +575,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
   const int all = npos > kCMaxList;
   int M = npos;
   if (!all) {
-    const int C = (npos + kGThreads - 1) / kGThreads;
+    const int C = (npos + kCThreads - 1) / kCThreads;
     const int p0 = min(npos, tid * C), p1 = min(npos, p0 + C);
     int cnt = 0;
     for (int p = p0; p < p1; ++p) cnt += (__ldg(P.x + p) != 0);
@@ -578,7 +589,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
     __syncthreads();
     int base = 0;
     M = 0;
-    for (int w2 = 0; w2 < kGWarps; ++w2) {
+    for (int w2 = 0; w2 < kCWarps; ++w2) {
       const int v = s_wsum[w2];
       if (w2 < warp) base += v;
       M += v;
@@ -589,8 +600,8 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
     __syncthreads();
   }
   const long long W = (long long)M * np;
-  const long long nwt = (long long)gridDim.x * kGWarps;
-  const long long gw = (long long)blockIdx.x * kGWarps + warp;
+  const long long nwt = (long long)gridDim.x * kCWarps;
+  const long long gw = (long long)blockIdx.x * kCWarps + warp;
   const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lo >= hi) return;
@@ -615,7 +626,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
     return;
   }
 
-  unsigned char* ring = smem_raw + (size_t)warp * kGStages * kPieceBytes;
+  unsigned char* ring = smem_raw + (size_t)warp * kCStages * kPieceBytes;
   CItem in = out;
   long long wi = lo;
   auto issue = [&](int s) {  // pieces of positions no longer masked are not read
@@ -629,7 +640,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
     }
   };
 #pragma unroll
-  for (int s = 0; s < kGStages - 1; ++s) {
+  for (int s = 0; s < kCStages - 1; ++s) {
     if (wi < hi) {
       issue(s);
       citem_next(in, all, s_list, M, Wn, np);
@@ -637,7 +648,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
     }
     cp_async_commit();
   }
-  int slot = 0, islot = kGStages - 1;
+  int slot = 0, islot = kCStages - 1;
   for (long long w = lo; w < hi; ++w) {
     if (out.b != seg.b || out.j != seg.j) {
       cseg_write(P, seg, lane);
@@ -649,7 +660,7 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
       ++wi;
     }
     cp_async_commit();
-    cp_async_wait_group<kGStages - 1>();
+    cp_async_wait_group<kCStages - 1>();
     if (seg.live) {
       const unsigned char* stage = ring + slot * kPieceBytes;
       const int ne = min(pe, P.V - out.k * pe);
@@ -663,8 +674,8 @@ __global__ void __launch_bounds__(kGThreads, 1) commit_stats_kernel(const __grid
       cseg_add(seg, out, r, P.bf16, pe, lane);
     }
     citem_next(out, all, s_list, M, Wn, np);
-    slot = (slot + 1 == kGStages) ? 0 : slot + 1;
-    islot = (islot + 1 == kGStages) ? 0 : islot + 1;
+    slot = (slot + 1 == kCStages) ? 0 : slot + 1;
+    islot = (islot + 1 == kCStages) ? 0 : islot + 1;
   }
   cseg_write(P, seg, lane);
   cp_async_wait_group<0>();
@@ -788,22 +799,22 @@ cudaError_t launch_commit(const DenseParams& p, float tau, int32_t* commit, floa
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(commit_stats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kGSmem);
+                             (int)kCSmem);
     if (e != cudaSuccess) return e;
     sms[dev] = n;
   }
   const long long pieces = (long long)p.B * (p.G + 1) * p.g.np;
   long long grid = sms[dev];
-  if (grid * kGWarps > pieces) grid = (pieces + kGWarps - 1) / kGWarps;
+  if (grid * kCWarps > pieces) grid = (pieces + kCWarps - 1) / kCWarps;
   DenseParams q = p;
-  q.stats_warps = grid * kGWarps;
+  q.stats_warps = grid * kCWarps;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t k1 = {};
   k1.gridDim = dim3((unsigned)grid, 1, 1);
-  k1.blockDim = dim3(kGThreads, 1, 1);
-  k1.dynamicSmemBytes = kGSmem;
+  k1.blockDim = dim3(kCThreads, 1, 1);
+  k1.dynamicSmemBytes = kCSmem;
   k1.stream = s;
   k1.attrs = attr;
   k1.numAttrs = 1;
