@@ -338,7 +338,7 @@ const char* spec_verify_status_string(int status);
  * on the warp-per-row path; 256 + 2 x 4 B + 32 B (gamma + 1) bytes (each
  * part rounded up to 256 bytes) on the single-pass path (17 KB at B = 64,
  * gamma = 7); on the two-kernel path 32 bytes per 2 KB piece of every row
- * and position plus small terms (0.33 MiB at B = 64, gamma = 7, V = 128256
+ * and position plus small terms (2.0 MiB at B = 64, gamma = 7, V = 128256
  * bf16).  Larger needs return SV_ERR_SCRATCH_LIMIT and launch nothing: sizes
  * that exceed the array on every path are refused on the host before any
  * CUDA call, the rest once the path is known.
