@@ -51,6 +51,7 @@ constexpr int kMaxChunks = 8;
 constexpr int kSliceBytes = 32 * 1024;     // preferred per-rank slice of one row (3 CTAs per SM)
 constexpr int kSliceCapBytes = 48 * 1024;  // largest slice (6 chunks)
 constexpr int kMaxCluster = 16;
+constexpr int kMaxPos = 256;  // positions per row (gamma + 1 <= 256)
 constexpr size_t kMaxDynSmem = 2 * (size_t)kSliceCapBytes + kSliceCapBytes / 4;  // rows + masses
 constexpr unsigned long long kWaitNs = 1000000000ull;  // bounded copy wait: one second
 
@@ -309,14 +310,23 @@ __device__ __forceinline__ Combined merge_parts(const float (*parts)[kPartWords]
 // row to arrive finalises it.  Warp 0 of the CTA that wrote the record.
 __device__ void arrive_and_finalize(const FusedParams& P, int b, int lane) {
   const int G = P.G;
+  // the row's draft tokens, read while the count is in flight (inputs: no
+  // ordering needed); lane l holds x_{l + 32 i} in xs[i]
+  int xs[(kMaxPos + 31) / 32];
+#pragma unroll
+  for (int i = 0; i < (kMaxPos + 31) / 32; ++i) {
+    const int jj = lane + 32 * i;
+    xs[i] = (jj < G) ? __ldg(P.x + (size_t)b * G + jj) : -1;
+  }
   unsigned old = 0;
   if (lane == 0) {
-    __threadfence();  // the record (written by this thread) before the count
-    old = atomicAdd(P.cnt + b, 1u);
+    // the record (written by this thread) released with the count; the last
+    // unit's count acquires every other unit's record
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(P.cnt + b) : "memory");
   }
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old != (unsigned)G) return;
-  __threadfence();  // every unit's record is visible once all have counted
+  __syncwarp();
   UnitRec* R = P.rec + (size_t)b * (G + 1);
   int n = G, err = 0, tmo = 0;
   for (int jj = lane; jj <= G; jj += 32) {
@@ -331,8 +341,11 @@ __device__ void arrive_and_finalize(const FusedParams& P, int b, int lane) {
   const bool bad = err || tmo;
   const int32_t tn = bad ? -1 : (int32_t)__ldcg(reinterpret_cast<const int*>(&R[n].token));
   int32_t* tok = P.tok_out + (size_t)b * (G + 1);
-  for (int jj = lane; jj <= G; jj += 32)
-    tok[jj] = bad ? -1 : (jj < n ? P.x[(size_t)b * G + jj] : (jj == n ? tn : -1));
+#pragma unroll
+  for (int i = 0; i < (kMaxPos + 31) / 32; ++i) {
+    const int jj = lane + 32 * i;
+    if (jj <= G) tok[jj] = bad ? -1 : (jj < n ? xs[i] : (jj == n ? tn : -1));
+  }
   // the records go back to zero, except the stop record that the
   // residual-output kernel reads (and clears) next
   for (int jj = lane; jj <= G; jj += 32)
