@@ -212,8 +212,13 @@ def test_anyorder_full_b4096_w32_v33():
     _anyorder_parity(wl.make("anyorder_b4096_w32_v33", seed=0))
 
 
-@pytest.mark.parametrize("B,D,W,V,dtype", [(64, 48, 16, 33, "f32"), (64, 32, 32, 27, "bf16"),
-                                           (32, 8, 5, 200, "f32")])
+@pytest.mark.parametrize("B,D,W,V,dtype", [
+    (64, 48, 16, 33, "f32"), (64, 32, 32, 27, "bf16"), (32, 8, 5, 200, "f32"),
+    # whole-window fp32 blocks copied in two groups (D = W, 16-byte multiples):
+    (50, 12, 12, 33, "f32"),    # a lane per row's statistics
+    (40, 4, 4, 101, "f32"),     # few long rows: the warp takes each row's statistics
+    (40, 8, 8, 1001, "f32"),
+])
 def test_anyorder_shapes(B, D, W, V, dtype):
     _anyorder_parity(wl.anyorder_inputs(B, D, W, V, dtype=dtype, seed=D + W + V))
 
