@@ -20,9 +20,13 @@
 //    the draft piece and folds them into the running statistics of the
 //    (b, j) segment it is in; the piece holding the draft token also gives
 //    the two logits there.  Each segment of a range ends in one 32-byte record
-//    at the segment's first piece.
+//    at the segment's first piece; when the range leaves a row (or ends) the
+//    warp adds its pieces of that row to the row's count (release).
 //  * dense_row_kernel: one thread-block cluster of C CTAs per row, launched
-//    as a programmatic dependent of the statistics kernel.  Every CTA finds
+//    as a programmatic dependent of the statistics kernel.  A CTA starts on
+//    its row once the row's count is complete (acquire; a row's pieces come
+//    from a few statistics CTAs, so most rows are decided while the grid
+//    still streams others).  Every CTA finds
 //    the row's records from the statistics warps' ranges, combines them per
 //    position (float-float), forms p/q at the draft token, runs the accept
 //    tests and takes the first rejection n and the draw constants.  Each CTA
@@ -73,6 +77,38 @@ __device__ __forceinline__ void zero32(T* p) {
   int4* q = reinterpret_cast<int4*>(p);
   q[0] = make_int4(0, 0, 0, 0);
   q[1] = make_int4(0, 0, 0, 0);
+}
+
+// Row b's count of pieces whose statistics records are written.  A
+// statistics warp adds its pieces of row b once the last of its records in
+// that row is stored (release); the row kernel's CTAs acquire the full count
+// (G + 1) np before they read the row's records, and the row's rank-0 CTA
+// clears it again.
+__device__ __forceinline__ uint32_t* row_count(const DenseParams& P, int b) {
+  return ws_at<uint32_t>(P, P.L.rcnt) + (size_t)b * kRowCountStride;
+}
+__device__ __forceinline__ void row_signal(const DenseParams& P, int b, long long pieces,
+                                           int lane) {
+  if (lane == 0)
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(row_count(P, b)),
+                 "r"((uint32_t)pieces)
+                 : "memory");
+}
+constexpr unsigned long long kRowWaitNs = 1000000000ull;  // one second
+// thread 0 of a row-kernel CTA: poll row b's count until it is complete, for
+// at most a second (and 2^22 polls); false when the wait ran out
+__device__ __noinline__ bool wait_row_ready(const DenseParams& P, int b) {
+  const uint32_t* c = row_count(P, b);
+  const uint32_t need = (uint32_t)(P.G + 1) * (uint32_t)P.g.np;
+  const unsigned long long deadline = globaltimer() + kRowWaitNs;
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= need) return true;
+    if (globaltimer() > deadline) return false;
+    __nanosleep(256);
+  }
+  return false;
 }
 
 __device__ __forceinline__ const unsigned char* target_row(const DenseParams& P, int b, int j) {
@@ -590,8 +626,8 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
   const long long nwt = (long long)gridDim.x * kStatsWarps;
   const long long gw = (long long)blockIdx.x * kStatsWarps + warp;
   const long long lo = gw * W / nwt, hi = (gw + 1) * W / nwt;
-  // the dependent row kernel may be scheduled as soon as SMs free up; it waits
-  // for this whole grid (and its memory) before it reads anything
+  // the dependent row kernel may be scheduled as soon as SMs free up; each of
+  // its CTAs waits for its row's count before it reads the row's records
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (lo >= hi) return;
   const uint32_t ninf = P.bf16 ? kNegInf2 : kNegInfF;
@@ -600,9 +636,14 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
     Item it = item_at(lo, G, np);
     SegAcc acc;
     seg_begin(acc, it, lo, P);
+    long long rstart = lo;  // this range's first piece in row acc.b
     for (long long w = lo; w < hi; ++w, item_next(it, G, np)) {
       if (it.b != acc.b || it.j != acc.j) {
         seg_write(P, acc, lane);
+        if (it.b != acc.b) {
+          row_signal(P, acc.b, w - rstart, lane);
+          rstart = w;
+        }
         seg_begin(acc, it, w, P);
       }
       const int ne = min(pe, P.V - it.k * pe);
@@ -616,6 +657,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
       piece_accumulate(P, it, rt, rd, lane, acc);
     }
     seg_write(P, acc, lane);
+    row_signal(P, acc.b, hi - rstart, lane);
     return;
   }
 
@@ -634,9 +676,14 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
   int slot = 0, islot = kStages - 1;
   SegAcc acc;
   seg_begin(acc, out, lo, P);
+  long long rstart = lo;  // this range's first piece in row acc.b
   for (long long w = lo; w < hi; ++w) {
     if (out.b != acc.b || out.j != acc.j) {
       seg_write(P, acc, lane);
+      if (out.b != acc.b) {  // the range has left row acc.b: its records are all stored
+        row_signal(P, acc.b, w - rstart, lane);
+        rstart = w;
+      }
       seg_begin(acc, out, w, P);
     }
     if (wi < hi) {
@@ -674,6 +721,7 @@ __global__ void __launch_bounds__(kStatsThreads, kStatsCtas) dense_stats_kernel(
     islot = (islot + 1 == kStages) ? 0 : islot + 1;
   }
   seg_write(P, acc, lane);
+  row_signal(P, acc.b, hi - rstart, lane);
   cp_async_wait_group<0>();
 }
 
@@ -1014,9 +1062,14 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
     F.x[j] = P.x[(size_t)b * G + j];
   }
   if (threadIdx.x == 0) F.us = P.u_s[b];
-  // ... then, launched as a programmatic dependent of the statistics kernel,
-  // wait for it to complete (and its records to be visible)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // ... then wait for the row's statistics alone: the count is complete once
+  // every statistics warp whose range meets the row has stored its records
+  // there (release by that warp, acquire here), often while the grid still
+  // streams later rows.  A launch as a programmatic dependent makes every
+  // statistics CTA resident before any CTA of this grid starts, so the wait
+  // needs nothing from this grid to end.
+  if (threadIdx.x == 0 && !wait_row_ready(P, b)) atomicOr(&hdr_of(P)->status, kStatusTimeout);
+  __syncthreads();
   finalize_row(P, b, warp, lane, F, owner);
   StopInfo st = F.st;
   // residual (or p) masses of this CTA's share of the stop position's pieces,
@@ -1081,8 +1134,12 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
     const int lo = (int)((long long)(r - 1) * nrec / (C - 1));
     const int hi = (int)((long long)r * nrec / (C - 1));
     for (int i = lo + (int)threadIdx.x; i < hi; i += kThreads) zero32(up_row + i);
+    // this grid completes only after the statistics grid (whatever follows
+    // on the stream may rely on both)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     return;
   }
+  if (threadIdx.x == 0) *row_count(P, b) = 0u;  // every CTA of the cluster has passed its wait
   // the draw; the masses kept off chip are consumed
   float* rm = ws_at<float>(P, P.L.rmass) + (size_t)b * P.g.np4;
   double T = 0.0;
@@ -1105,6 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
     st.T = T;
     ws_at<StopInfo>(P, P.L.stop)[b] = st;
   }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 // residual_out: the distribution the emitted token was drawn from.  One CTA

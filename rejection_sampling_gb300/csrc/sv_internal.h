@@ -68,8 +68,13 @@ struct StopInfo {
 };
 
 struct DenseLayout {  // byte offsets into the workspace
-  size_t upart, stop, rmass, total;
+  size_t upart, stop, rmass, rcnt, total;
 };
+
+// per row: the count of its pieces whose statistics are written, one counter
+// per 128-byte line (the row kernel's waits poll them while the statistics
+// grid streams)
+constexpr int kRowCountStride = 32;  // uint32 words
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -82,6 +87,8 @@ inline DenseLayout dense_layout(long long B, int G, const DenseGeom& g) {
   o = align_up(o + sizeof(StopInfo) * (size_t)B, 256);
   L.rmass = o;
   o = align_up(o + sizeof(float) * (size_t)B * (size_t)g.np4, 256);
+  L.rcnt = o;
+  o = align_up(o + sizeof(uint32_t) * kRowCountStride * (size_t)B, 256);
   L.total = o;
   return L;
 }
