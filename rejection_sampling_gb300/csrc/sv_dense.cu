@@ -102,9 +102,14 @@ __device__ __noinline__ bool wait_row_ready(const DenseParams& P, int b) {
   const uint32_t need = (uint32_t)(P.G + 1) * (uint32_t)P.g.np;
   const unsigned long long deadline = globaltimer() + kRowWaitNs;
   for (uint32_t i = 0; i < (1u << 22); ++i) {
+    // relaxed polls (an acquire load per poll costs the SM more), then one
+    // acquire load of the complete count
     uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-    if (v >= need) return true;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= need) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      return true;
+    }
     if (globaltimer() > deadline) return false;
     __nanosleep(256);
   }
