@@ -45,14 +45,18 @@
  *     contains NaN or +inf or is entirely -inf) do not stop the call: the
  *     offending row gets n_accepted = -1 and out_tokens = -1, and a bit is
  *     set in the workspace status word that spec_verify_check() reports.
- *   - Waits between thread blocks are only the hardware's: the dense
- *     kernels are programmatic dependents (griddepcontrol.wait) of whatever
- *     precedes them on the stream and read nothing before that grid has
- *     completed; the CTAs of a thread-block cluster meet at cluster
- *     barriers.  No kernel spins on memory written by another block.  The
- *     single-pass dense kernel waits on its own bulk copies into shared
- *     memory, for about one second at most: a copy that has not landed by
- *     then gives its row n_accepted = -1 and sets the timeout bit, which
+ *   - Waits between thread blocks: the dense kernels are programmatic
+ *     dependents (griddepcontrol.wait) of whatever precedes them on the
+ *     stream and read nothing that grid writes before it has completed; the
+ *     CTAs of a thread-block cluster meet at cluster barriers.  One kernel
+ *     polls memory written by another grid: the row kernel of the two-kernel
+ *     dense path waits for its row's piece count, which the statistics
+ *     kernel's warps raise as they store the row's statistics.  Its launch as
+ *     a programmatic dependent makes every statistics block resident before
+ *     any row block starts, so the count always completes.  The single-pass
+ *     dense kernel waits on its own bulk copies into shared memory.  Each of
+ *     these waits gives up after about one second: the row then gets
+ *     n_accepted = -1 and out_tokens = -1 and the timeout bit is set, which
  *     spec_verify_check reports as SV_ERR_TIMEOUT.
  */
 #ifndef SPEC_VERIFY_H
@@ -75,7 +79,7 @@ typedef enum sv_status {
   SV_ERR_UNSUPPORTED = 2,  /* valid request this build cannot run (e.g. no GPU) */
   SV_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed             */
   SV_ERR_DEVICE_INPUT = 4, /* spec_verify_check: some row had invalid inputs   */
-  SV_ERR_TIMEOUT = 5,      /* spec_verify_check: a bounded copy wait ran out */
+  SV_ERR_TIMEOUT = 5,      /* spec_verify_check: a bounded wait ran out */
   SV_ERR_SCRATCH_LIMIT = 6 /* spec_verify_dense_static: sizes need more scratch
                               than SV_STATIC_SCRATCH_BYTES; nothing launched  */
 } sv_status;
@@ -307,8 +311,8 @@ int spec_support_topk(const void* logits, sv_dtype dtype, int N, int V, float te
 
 /*
  * spec_verify_check -- synchronise `stream`, read and clear the workspace
- * status word.  Returns SV_OK, SV_ERR_TIMEOUT (a bulk copy of the single-pass
- * dense kernel did not land within its bounded wait; that row carries
+ * status word.  Returns SV_OK, SV_ERR_TIMEOUT (a dense row's statistics or
+ * bulk copies did not arrive within the bounded wait; that row carries
  * n_accepted = -1), SV_ERR_DEVICE_INPUT (some row of an earlier call had
  * invalid inputs; those rows carry n_accepted = -1), or SV_ERR_CUDA.
  */
@@ -352,8 +356,8 @@ const char* spec_verify_status_string(int status);
  *     host threads) race on the array and must be ordered by the caller.
  *   - Errors: host-side argument errors as spec_verify_dense (nothing
  *     launched).  There is no status word to query: rows with invalid inputs
- *     (and, on the single-pass path, rows whose bulk copy did not land
- *     within the bounded wait) carry n_accepted = -1.
+ *     (and rows whose statistics or bulk copies did not arrive within the
+ *     bounded wait) carry n_accepted = -1.
  */
 #define SV_STATIC_SCRATCH_BYTES (4u << 20)
 int spec_verify_dense_static(const void* target_logits, const void* draft_logits, sv_dtype dtype,

@@ -375,6 +375,7 @@ struct FinShared {
   int x[kMaxG];       // draft tokens of the row (prefetched)
   int n;              // first rejected position (G + 1: none)
   int err;
+  int tmo;            // the wait for the row's statistics ran out
   float us;           // u_sample of the row (prefetched)
   StopInfo st;        // the result: stop position and its draw constants
 };
@@ -396,7 +397,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
   const unsigned W32 = (unsigned)W, n32 = (unsigned)nwt;
   if (threadIdx.x == 0) {
     F.n = G + 1;
-    F.err = 0;
+    F.err = F.tmo;  // a row whose statistics never arrived is failed like an input error
   }
   __syncthreads();
   for (int j = warp; j <= G; j += kWarps) {
@@ -468,7 +469,7 @@ __device__ void finalize_row(const DenseParams& P, int b, int warp, int lane, Fi
     if (err) {
       st.mode = 2;
       st.ct = st.cd = st.invSt = st.invSd = 0.f;
-      if (owner) atomicOr(&hdr_of(P)->status, kStatusInputErr);
+      if (owner) atomicOr(&hdr_of(P)->status, F.tmo ? kStatusTimeout : kStatusInputErr);
     } else if (n < G) {
       st.mode = 0;
       st.ct = F.c[0][n];
@@ -1073,7 +1074,7 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
   // streams later rows.  A launch as a programmatic dependent makes every
   // statistics CTA resident before any CTA of this grid starts, so the wait
   // needs nothing from this grid to end.
-  if (threadIdx.x == 0 && !wait_row_ready(P, b)) atomicOr(&hdr_of(P)->status, kStatusTimeout);
+  if (threadIdx.x == 0) F.tmo = wait_row_ready(P, b) ? 0 : 1;
   __syncthreads();
   finalize_row(P, b, warp, lane, F, owner);
   StopInfo st = F.st;
