@@ -161,6 +161,42 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, unsigned by
       : "memory");
 }
 
+// Row b's count of pieces whose statistics records are stored (the dense
+// two-kernel path; one counter per 128-byte line).  A statistics warp adds
+// its pieces of row b once the last of its records in that row is stored
+// (release); the row kernel's thread 0 waits for the complete count before
+// the row's records are read, and the row kernel clears it again.
+__device__ __forceinline__ uint32_t* row_count(const DenseParams& P, int b) {
+  return reinterpret_cast<uint32_t*>(P.ws + P.L.rcnt) + (size_t)b * kRowCountStride;
+}
+__device__ __forceinline__ void row_signal(const DenseParams& P, int b, long long pieces,
+                                           int lane) {
+  if (lane == 0)
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(row_count(P, b)),
+                 "r"((uint32_t)pieces)
+                 : "memory");
+}
+constexpr unsigned long long kRowWaitNs = 1000000000ull;  // one second
+// Poll row b's count until it reaches `need`: relaxed loads 256 ns apart
+// (an acquire load per poll costs the SM more), then one acquire load of the
+// complete count.  At most a second of globaltimer and 2^22 polls; false when
+// the wait ran out.
+static __device__ __noinline__ bool wait_row_ready(const DenseParams& P, int b, uint32_t need) {
+  const uint32_t* c = row_count(P, b);
+  const unsigned long long deadline = globaltimer() + kRowWaitNs;
+  for (uint32_t i = 0; i < (1u << 22); ++i) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= need) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+      return true;
+    }
+    if (globaltimer() > deadline) return false;
+    __nanosleep(256);
+  }
+  return false;
+}
+
 // ---------------------------------------------------------------------------
 // float-float arithmetic (a value is hi + lo with |lo| <= ulp(hi)/2).
 // GB300's fp64 pipe is a small fraction of its fp32 rate, so sums that need

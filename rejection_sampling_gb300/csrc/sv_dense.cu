@@ -79,43 +79,6 @@ __device__ __forceinline__ void zero32(T* p) {
   q[1] = make_int4(0, 0, 0, 0);
 }
 
-// Row b's count of pieces whose statistics records are written.  A
-// statistics warp adds its pieces of row b once the last of its records in
-// that row is stored (release); the row kernel's CTAs acquire the full count
-// (G + 1) np before they read the row's records, and the row's rank-0 CTA
-// clears it again.
-__device__ __forceinline__ uint32_t* row_count(const DenseParams& P, int b) {
-  return ws_at<uint32_t>(P, P.L.rcnt) + (size_t)b * kRowCountStride;
-}
-__device__ __forceinline__ void row_signal(const DenseParams& P, int b, long long pieces,
-                                           int lane) {
-  if (lane == 0)
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(row_count(P, b)),
-                 "r"((uint32_t)pieces)
-                 : "memory");
-}
-constexpr unsigned long long kRowWaitNs = 1000000000ull;  // one second
-// thread 0 of a row-kernel CTA: poll row b's count until it is complete, for
-// at most a second (and 2^22 polls); false when the wait ran out
-__device__ __noinline__ bool wait_row_ready(const DenseParams& P, int b) {
-  const uint32_t* c = row_count(P, b);
-  const uint32_t need = (uint32_t)(P.G + 1) * (uint32_t)P.g.np;
-  const unsigned long long deadline = globaltimer() + kRowWaitNs;
-  for (uint32_t i = 0; i < (1u << 22); ++i) {
-    // relaxed polls (an acquire load per poll costs the SM more), then one
-    // acquire load of the complete count
-    uint32_t v;
-    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-    if (v >= need) {
-      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
-      return true;
-    }
-    if (globaltimer() > deadline) return false;
-    __nanosleep(256);
-  }
-  return false;
-}
-
 __device__ __forceinline__ const unsigned char* target_row(const DenseParams& P, int b, int j) {
   return P.lt + ((size_t)b * (P.G + 1) + j) * (size_t)P.V * P.g.es;
 }
@@ -1063,18 +1026,19 @@ __global__ void __launch_bounds__(kThreads, 2) dense_row_kernel(const __grid_con
   // leave (it waits for this grid before it reads anything)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // inputs first (they do not come from the statistics kernel) ...
+  // (read from L2: this grid does not wait for the grids before it)
   for (int j = threadIdx.x; j < G; j += kThreads) {
-    F.u[j] = P.u_acc[(size_t)b * G + j];
-    F.x[j] = P.x[(size_t)b * G + j];
+    F.u[j] = __ldcg(P.u_acc + (size_t)b * G + j);
+    F.x[j] = __ldcg(P.x + (size_t)b * G + j);
   }
-  if (threadIdx.x == 0) F.us = P.u_s[b];
+  if (threadIdx.x == 0) F.us = __ldcg(P.u_s + b);
   // ... then wait for the row's statistics alone: the count is complete once
   // every statistics warp whose range meets the row has stored its records
   // there (release by that warp, acquire here), often while the grid still
   // streams later rows.  A launch as a programmatic dependent makes every
   // statistics CTA resident before any CTA of this grid starts, so the wait
   // needs nothing from this grid to end.
-  if (threadIdx.x == 0) F.tmo = wait_row_ready(P, b) ? 0 : 1;
+  if (threadIdx.x == 0) F.tmo = wait_row_ready(P, b, (uint32_t)(G + 1) * (uint32_t)np) ? 0 : 1;
   __syncthreads();
   finalize_row(P, b, warp, lane, F, owner);
   StopInfo st = F.st;
