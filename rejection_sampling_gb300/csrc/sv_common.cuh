@@ -19,9 +19,18 @@ namespace sv {
 constexpr float kLog2e = 1.44269504088896340736f;
 
 // ---------------------------------------------------------------------------
-// fast exp2 (MUFU.EX2): ex2.approx.ftz.f32, hardware instruction
+// fast exp2 (MUFU.EX2): ex2.approx.ftz.f32, hardware instruction.  ex2 may be
+// scheduled freely; ex2_ordered stays in program order with the other
+// volatile asm (copy issue, waits), which the dense statistics stream
+// measured faster with (its loads stay ahead of the arithmetic), while the
+// warp-per-row and commit kernels measured faster with the free form.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float ex2_ordered(float x) {
   float y;
   asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
@@ -70,6 +79,11 @@ __device__ __forceinline__ f32x2 f2_exp2_shift(f32x2 a, f32x2 L, f32x2 nc) {
   float y0, y1;
   f2_unpack(f2_fma(a, L, nc), y0, y1);
   return f2_pack(ex2(y0), ex2(y1));
+}
+__device__ __forceinline__ f32x2 f2_exp2_shift_ordered(f32x2 a, f32x2 L, f32x2 nc) {
+  float y0, y1;
+  f2_unpack(f2_fma(a, L, nc), y0, y1);
+  return f2_pack(ex2_ordered(y0), ex2_ordered(y1));
 }
 // a bf16 pair in one 32-bit word as an fp32 pair (exact)
 __device__ __forceinline__ f32x2 f2_bf16(uint32_t w) {

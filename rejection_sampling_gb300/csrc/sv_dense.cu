@@ -99,9 +99,9 @@ __device__ __forceinline__ float part_scale(float c, float C) { return scale_exa
 // masses and the final walk see bit-identical values.
 __device__ __forceinline__ float resid_val(float t, float d, float ct, float cd, float invSt,
                                            float invSd, int mode) {
-  const float p = __fmul_rn(ex2(__fmaf_rn(t, kLog2e, -ct)), invSt);
+  const float p = __fmul_rn(ex2_ordered(__fmaf_rn(t, kLog2e, -ct)), invSt);
   if (mode != 0) return p;
-  const float q = __fmul_rn(ex2(__fmaf_rn(d, kLog2e, -cd)), invSd);
+  const float q = __fmul_rn(ex2_ordered(__fmaf_rn(d, kLog2e, -cd)), invSd);
   const float r = __fsub_rn(p, q);
   return r > 0.f ? r : 0.f;
 }
@@ -194,16 +194,16 @@ __device__ __forceinline__ void lane_fold(const uint4 (&r)[4], int bf16, float& 
   if (bf16) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].x), L2, nc));
-      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].y), L2, nc));
-      a01 = f2_add(a01, f2_exp2_shift(f2_bf16(r[i].z), L2, nc));
-      a23 = f2_add(a23, f2_exp2_shift(f2_bf16(r[i].w), L2, nc));
+      a01 = f2_add(a01, f2_exp2_shift_ordered(f2_bf16(r[i].x), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift_ordered(f2_bf16(r[i].y), L2, nc));
+      a01 = f2_add(a01, f2_exp2_shift_ordered(f2_bf16(r[i].z), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift_ordered(f2_bf16(r[i].w), L2, nc));
     }
   } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      a01 = f2_add(a01, f2_exp2_shift(f2_pack(__uint_as_float(r[i].x), __uint_as_float(r[i].y)), L2, nc));
-      a23 = f2_add(a23, f2_exp2_shift(f2_pack(__uint_as_float(r[i].z), __uint_as_float(r[i].w)), L2, nc));
+      a01 = f2_add(a01, f2_exp2_shift_ordered(f2_pack(__uint_as_float(r[i].x), __uint_as_float(r[i].y)), L2, nc));
+      a23 = f2_add(a23, f2_exp2_shift_ordered(f2_pack(__uint_as_float(r[i].z), __uint_as_float(r[i].w)), L2, nc));
     }
   }
   float a0, a1, a2, a3;

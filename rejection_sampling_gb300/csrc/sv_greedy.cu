@@ -629,8 +629,8 @@ __global__ void __launch_bounds__(kCThreads, 1) commit_stats_kernel(const __grid
   unsigned char* ring = smem_raw + (size_t)warp * kCStages * kPieceBytes;
   CItem in = out;
   long long wi = lo;
-  auto issue = [&](int s) {  // pieces of positions no longer masked are not read
-    if (!is_masked(P, in.b, in.j)) return;
+  auto issue = [&](int s) {  // a full sweep does not read the unmasked positions' pieces
+    if (all && !is_masked(P, in.b, in.j)) return;
     const int ne = min(pe, P.V - in.k * pe);
     const unsigned char* src = target_row(P, in.b, in.j) + (size_t)in.k * kPieceBytes;
 #pragma unroll
