@@ -419,6 +419,7 @@ __device__ __forceinline__ bool is_masked(const DenseParams& P, int b, int j) {
 }
 
 constexpr int kCMaxList = 8192;  // positions whose masked subset is listed in shared memory
+constexpr int kCSlots = 5;       // record slots per lane in flight in the commit row kernel
 // The commit statistics kernel's geometry (the greedy sweep's: measured
 // against 12 x 8, 16 x 6 and 24 x 4 warps x stages, all slower)
 constexpr int kCWarps = 24;
@@ -708,10 +709,12 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
     float m = -INFINITY;
     ff S{0.f, 0.f};
     int idx = INT_MAX, bad = 0;
-    for (int k0 = lane; k0 < np; k0 += 4 * 32) {  // four slots per lane in flight at once
-      int4 v0[4], v1[4];
+    // five slots per lane in flight at once: one round for the 148-149
+    // pieces of a 128k-152k vocabulary
+    for (int k0 = lane; k0 < np; k0 += kCSlots * 32) {
+      int4 v0[kCSlots], v1[kCSlots];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kCSlots; ++u) {
         v1[u] = make_int4(0, 0, 0, 0);
         if (k0 + 32 * u < np) {
           const int4* rp = reinterpret_cast<const int4*>(rec + P0 + k0 + 32 * u);
@@ -720,7 +723,7 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
         }
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < kCSlots; ++u) {
         if (v1[u].y != 1) continue;
         int4* rp = reinterpret_cast<int4*>(rec + P0 + k0 + 32 * u);
         rp[0] = make_int4(0, 0, 0, 0);
