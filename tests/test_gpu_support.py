@@ -129,3 +129,29 @@ def test_support_sorted_rows(dtype):
     a = wl.bf16_bits(rows) if dtype == "bf16" else rows
     for K in (1, 50, 200):
         support_parity(a, 1.0, K, 0.913, min_clean=0.5)
+
+
+def test_support_full_960_rows():
+    # the support workload at full size: all 960 target and draft rows of a
+    # headline batch (one full wave of CTAs and part of a second)
+    d = wl.make("dense_b64_g7_v128256", seed=1)
+    rows = np.concatenate([d["target"].reshape(-1, d["V"]), d["draft"].reshape(-1, d["V"])])
+    support_parity(rows, 1.0, 50, 0.95)
+
+
+def test_support_input_errors_in_the_last_wave():
+    # errors in the last rows of a 960-row call (CTAs of the second wave): a
+    # NaN early and one late in the row, +inf, a row of -inf
+    N, V = 960, 60000
+    a = _normal_rows(N, V, "f32", seed=9)
+    a[N - 1, 100] = np.nan
+    a[N - 2, 7000] = np.nan
+    a[N - 3, V - 1] = np.inf
+    a[N - 4, :] = -np.inf
+    b = wl.bf16_bits(a)
+    ids, probs = run_support(b, 1.0, 50, 0.95)
+    assert (ids[N - 4:] == -1).all() and np.isnan(probs[N - 4:]).all()
+    assert rs.check() == rs.SV_ERR_DEVICE_INPUT
+    o = oracle.support_topk(b[:N - 4], 1.0, 50, 0.95)
+    np.testing.assert_array_equal(ids[:N - 4], o["ids"])
+    assert rs.check() == rs.SV_OK
