@@ -38,6 +38,7 @@ constexpr int kLWarps = 4;  // sequences (warps) per CTA of the lane-per-positio
 constexpr int kLThreads = 32 * kLWarps;
 constexpr int kDraftCache = 1024;  // window positions whose draft statistics are kept
 constexpr int kLaneMaxV = 512;     // vocabularies a lane reduces alone
+constexpr int kXC = 4;             // rounds whose inputs a lane keeps (the one-group fast path)
 
 __device__ __forceinline__ float logit_at(const unsigned char* row, int y, int bf16) {
   if (bf16) return bf16_to_f32(reinterpret_cast<const uint16_t*>(row)[y]);
@@ -314,7 +315,12 @@ __device__ __forceinline__ Stats row_stats_lane_staged(const unsigned char* row,
 // round needs no block barrier; the whole warp then draws.
 __global__ void __launch_bounds__(kLThreads) rounds_lane_kernel(const __grid_constant__ RoundsParams P) {
   __shared__ float s_rowbuf[kLWarps * 32 * 33];
-  const int lane = threadIdx.x & 31;
+  // one-group fast path: per lane, every round's draft token, accept uniform
+  // and the draft logit at that token
+  __shared__ int s_xr[kLWarps][kXC][32];
+  __shared__ float s_ua[kLWarps][kXC][32];
+  __shared__ float s_dx[kLWarps][kXC][32];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
   float* const rslot = s_rowbuf + (threadIdx.x >> 5) * 32 * 33 + lane * 33;
   const bool staged = !P.bf16 && P.V <= 32;  // fp32 rows short enough to stage
   const int b = blockIdx.x * kLWarps + (threadIdx.x >> 5);
@@ -328,8 +334,10 @@ __global__ void __launch_bounds__(kLThreads) rounds_lane_kernel(const __grid_con
   int bad = (i0 < 0 || i0 > D || W < 1);
   const int e = bad ? 0 : ((W > D - i0) ? D : i0 + W);
   int odd = 0;
+  int s0 = 0;  // sigma of this lane's slot in group 0 (sigma index i0 + lane)
   for (int k = i0 + lane; k < e; k += 32) {
     const int s = sig[k];
+    if (k == i0 + lane) s0 = s;
     odd |= (s < 0 || s >= D);
     for (int k2 = i0; k2 < k && !odd; ++k2) odd |= (sig[k2] == s);
   }
@@ -340,7 +348,79 @@ __global__ void __launch_bounds__(kLThreads) rounds_lane_kernel(const __grid_con
   Stats dcache;  // the draft statistics of this lane's slot in group 0
   int have = 0;
   int i = i0;
-  for (int r = 0; r < R; ++r) {
+  // The fast path (fp32 rows of at most 32 logits, a window of at most 32
+  // positions, at most kXC rounds): the lane loads every round's draft token
+  // and uniform for its slot at once, stages its draft row first and reads
+  // the draft logits at those tokens from it; a round is then one staging of
+  // its target rows (the target logit at the token read from the stage), the
+  // ballot and the draw, and the accepted prefix is written from registers.
+  const bool fast = staged && !bad && R <= kXC && e - i0 <= 32;  // warp-uniform
+  if (fast && i0 + lane < e) {
+    int xv[kXC];
+    float uv[kXC];
+#pragma unroll
+    for (int r = 0; r < kXC; ++r) {
+      if (r < R) {
+        const size_t rr = ((size_t)b * R + r) * (size_t)D;
+        xv[r] = P.x[rr + s0];
+        uv[r] = P.u_acc[rr + i0 + lane];
+      }
+    }
+    dcache = row_stats_lane_staged(P.ld + ((size_t)b * D + s0) * (size_t)V * es, V, rslot);
+    have = 1;
+#pragma unroll
+    for (int r = 0; r < kXC; ++r) {
+      if (r < R) {
+        s_xr[wi][r][lane] = xv[r];
+        s_ua[wi][r][lane] = uv[r];
+        s_dx[wi][r][lane] = (xv[r] >= 0 && xv[r] < V) ? rslot[xv[r]] : 0.f;
+      }
+    }
+  }
+  __syncwarp();
+  for (int r = 0; fast && r < R; ++r) {
+    if (bad || i >= e) break;  // warp-uniform
+    const size_t rr = ((size_t)b * R + r) * (size_t)D;
+    const int k = i0 + lane;
+    const bool active = (k >= i) && (k < e);
+    int res = 0;
+    Stats t{0.f, 1.f, 0};
+    const Stats d = dcache;
+    if (active) {
+      t = row_stats_lane_staged(P.lt + (rr + s0) * (size_t)V * es, V, rslot);
+      const int x = s_xr[wi][r][lane];
+      res = 2;
+      if (!t.bad && !d.bad && x >= 0 && x < V) {
+        const float a = accept_prob(rslot[x], s_dx[wi][r][lane], t, d);
+        res = (s_ua[wi][r][lane] < a) ? 0 : 1;
+      }
+    }
+    const unsigned nacc = __ballot_sync(0xffffffffu, active && res != 0);
+    int stop = e;
+    if (nacc) {
+      const int j = __ffs(nacc) - 1;
+      stop = i0 + j;
+      if (__shfl_sync(0xffffffffu, res, j) == 2) {
+        bad = 1;
+        break;
+      }
+      const float tc = __shfl_sync(0xffffffffu, t.c, j), tS = __shfl_sync(0xffffffffu, t.S, j);
+      const float dc = __shfl_sync(0xffffffffu, d.c, j), dS = __shfl_sync(0xffffffffu, d.S, j);
+      const int s = __shfl_sync(0xffffffffu, s0, j);
+      if (active && k < stop) out[s0] = s_xr[wi][r][lane];
+      if (lane == 0) racc[r] = stop - i;
+      const int y = warp_draw(P.lt + (rr + s) * (size_t)V * es, P.ld + ((size_t)b * D + s) * (size_t)V * es,
+                              V, P.bf16, tc, tS, dc, dS, P.u_s[(size_t)b * R + r], lane);
+      if (lane == 0) out[s] = y;
+      i = stop + 1;
+    } else {
+      if (active) out[s0] = s_xr[wi][r][lane];
+      if (lane == 0) racc[r] = stop - i;
+      i = e;
+    }
+    __syncwarp();
+  }
+  for (int r = 0; !fast && r < R; ++r) {
     if (bad || i >= e) break;  // warp-uniform
     const size_t rr = ((size_t)b * R + r) * (size_t)D;
     int stop = e, err = 0;

@@ -59,6 +59,7 @@ def rounds_parity(d, window, min_clean=0.9):
 
 @pytest.mark.parametrize("B,R,D,V,dtype,wmax", [
     (64, 4, 32, 33, "f32", 32),       # the any-order shape, every window length
+    (64, 4, 40, 32, "f32", 32),       # the one-group fast path at its limits (V, R, window)
     (128, 3, 256, 27, "bf16", 24),    # text8-like
     (16, 2, 40, 1000, "f32", 40),     # rows longer than a warp's stride
     (6, 2, 20, 50000, "bf16", 12),    # a large vocabulary
