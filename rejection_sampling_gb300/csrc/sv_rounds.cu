@@ -14,7 +14,11 @@
 // every round in one launch; lane j takes window slot j of the current group
 // of 32, forms its rows' statistics alone and keeps its draft statistics in
 // registers; a ballot finds the round's first position that is not accepted,
-// so nothing synchronises the block.
+// so nothing synchronises the block.  fp32 rows of at most 32 logits in a
+// window of at most 32 positions (and at most kXC rounds) take a shorter
+// chain: each lane loads every round's draft token and uniform for its slot
+// at once and reads the draft logits at those tokens from its staged draft
+// row, so a round is one staging of its target rows, the ballot and the draw.
 //
 // Design, larger vocabularies (rounds_kernel): one CTA of 8 warps per
 // sequence, every round in one launch.  A round takes its positions eight at
