@@ -301,12 +301,17 @@ __global__ void __launch_bounds__(kGThreads, 1) greedy_stats_kernel(const __grid
 __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __grid_constant__ DenseParams P) {
   __shared__ int s_n, s_err;
   __shared__ int s_arg[kGMaxPos];
+  __shared__ int s_x[kGMaxPos];  // the row's draft tokens
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x, G = P.G, np = P.g.np;
   if (threadIdx.x == 0) {
     s_n = G;
     s_err = 0;
   }
+  // the draft tokens first: an input, not a result of the statistics grid
+  // (this grid starts once every statistics CTA has passed its own wait for
+  // the grids before it; read from L2)
+  for (int j = threadIdx.x; j < G; j += blockDim.x) s_x[j] = __ldcg(P.x + (size_t)b * G + j);
   // the statistics grid's records must be complete and visible
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
@@ -319,7 +324,7 @@ __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __gri
   const bool idx32 = (unsigned long long)(nwt + 1) * (unsigned long long)(W + 1) < (1ull << 32);
   const unsigned W32 = (unsigned)W, n32 = (unsigned)nwt;
   for (int j = warp; j <= G; j += kGRowWarps) {
-    const int xj = (j < G) ? P.x[(size_t)b * G + j] : 0;
+    const int xj = (j < G) ? s_x[j] : 0;
     const long long P0 = ((long long)b * (G + 1) + j) * np, P1 = P0 + np;
     const long long g0 = idx32 ? (long long)(((unsigned)(P0 + 1) * n32 + W32 - 1) / W32) - 1
                                : ((P0 + 1) * nwt + W - 1) / W - 1;
@@ -363,7 +368,7 @@ __global__ void __launch_bounds__(32 * kGRowWarps) greedy_row_kernel(const __gri
   int32_t* tok = P.tok_out + (size_t)b * (G + 1);
   for (int j = threadIdx.x; j <= G; j += blockDim.x) {
     int v = -1;
-    if (!err) v = (j < n) ? P.x[(size_t)b * G + j] : (j == n ? s_arg[n] : -1);
+    if (!err) v = (j < n) ? s_x[j] : (j == n ? s_arg[n] : -1);
     tok[j] = v;
   }
   if (threadIdx.x == 0) {
@@ -687,15 +692,20 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
                                                                     float* confidence) {
   __shared__ float s_conf[kGMaxPos];
   __shared__ int s_tok[kGMaxPos];
+  __shared__ int s_msk[kGMaxPos];  // the block's mask flags
   __shared__ int s_err;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = blockIdx.x, G = P.G, Wn = G + 1, np = P.g.np;
   if (threadIdx.x == 0) s_err = 0;
+  // the mask flags first: an input, not a result of the statistics grid (this
+  // grid starts once every statistics CTA has passed its own wait for the
+  // grids before it; read from L2)
+  for (int j = threadIdx.x; j < Wn; j += blockDim.x) s_msk[j] = __ldcg(P.x + (size_t)b * Wn + j) != 0;
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   ConfRec* rec = reinterpret_cast<ConfRec*>(P.ws + P.L.upart);
   for (int j = warp; j < Wn; j += kGRowWarps) {
-    const bool masked = P.x[(size_t)b * Wn + j] != 0;
+    const bool masked = s_msk[j] != 0;
     if (!masked) {  // no record was written for it
       if (lane == 0) {
         s_conf[j] = -1.f;
@@ -769,7 +779,7 @@ __global__ void __launch_bounds__(32 * kGRowWarps) commit_row_kernel(const __gri
     float bc = -1.f;
     for (int j = 0; j < Wn; ++j) {
       const float c = s_conf[j];
-      const bool masked = P.x[(size_t)b * Wn + j] != 0;
+      const bool masked = s_msk[j] != 0;
       const int on = !err && masked && c > tau;
       cm[j] = err ? -1 : on;
       tk[j] = on ? s_tok[j] : -1;
